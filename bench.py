@@ -1,0 +1,486 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV decode hot path on GB300.
+
+One step = one pass of the hot path over one batch: the new token of every
+sequence is scattered into its slot (pa_reshape_and_cache), then paged
+decode attention runs over the whole context (pa_decode, context split across
+CTAs and merged by log-sum-exp in the last CTA). The default workload is the
+Qwen3-8B-shaped layer: 16 sequences x 4,164 tokens, 32 query / 8 KV heads,
+head_dim 128, bf16, blocks of 16 scattered over a 38,348-block pool.
+
+Prints ONE JSON line (rank 0). ``value`` is KV GB/s: the bytes of K and V a
+decode step must read (valid tokens only) divided by the device time per step,
+with inputs resident in HBM. Two batches alternate so that consecutive steps
+read disjoint 273 MB sets (L2 is 129 MB). ``e2e`` repeats the measurement
+through the public API with the step's inputs copied from pinned host memory
+and the output read back every step.
+
+``--impl reference`` times the oracle (fp64 CPU) on the host cores instead,
+one bounded sample of the workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+HBM_NOMINAL_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# workload description
+# ---------------------------------------------------------------------------
+def build_workload(config: str, rank: int, copies: int):
+    if config == "qwen3":
+        return workloads.qwen3(num_seqs=16, copies=copies), "qwen3-8b layer: 16 seqs x 4164 tokens, Hq 32, Hkv 8, D 128, bf16, block 16, pool 38348 blocks"
+    if config == "long":
+        return workloads.long_context(block_size=16, num_seqs=4 * copies), "long context: 4 seqs x 32768 tokens, Hq 64, Hkv 8, D 128, bf16, block 16"
+    if config == "gqa":
+        return workloads.gqa(num_seqs=64 * copies, num_blocks=20000 * copies), "llama gqa: 64 seqs, len U[512,4096], Hq 32, Hkv 8, D 128, bf16, block 16"
+    raise SystemExit(f"unknown config {config}")
+
+
+def per_batch(config: str) -> int:
+    return {"qwen3": 16, "long": 4, "gqa": 64}[config]
+
+
+def kv_bytes(lens, hkv, d, elem) -> int:
+    return int(sum(int(n) for n in lens)) * hkv * d * elem * 2
+
+
+def decode_alg_bytes(lens, hq, hkv, d, bs, elem) -> int:
+    """Algorithmic bytes of one decode launch: K/V of valid tokens, the query,
+    the fp32 output, the block-table entries used and the lengths."""
+    B = len(lens)
+    tbl = sum(workloads.cdiv(int(n), bs) for n in lens) * 4
+    return kv_bytes(lens, hkv, d, elem) + B * hq * d * elem + B * hq * d * 4 + tbl + B * 4
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("decode_mma.cu", "device_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_121_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"pa_decode_{config}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != decode_source_sha():
+        return None
+    return float(m_tr.group(1))
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled by nvidia-smi during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for t, line in self.lines:
+            if not (t0 <= t <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch, local_rank: int) -> str:
+    """Identifier nvidia-smi -i accepts for the GPU this process uses."""
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        if u and u != "None":
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip()]
+    return ids[local_rank].strip() if local_rank < len(ids) else str(local_rank)
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_units_time(batch, seqs, nthreads):
+    import oracle
+    q = batch.query[seqs]
+    tables = batch.block_tables[seqs]
+    lens = batch.context_lens[seqs]
+    t = time.perf_counter()
+    oracle.paged_attention(q, batch.k_cache, batch.v_cache, tables, lens, batch.scale,
+                           nthreads=nthreads)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(batch, nseq_batch, budget_s=10.0):
+    """The oracle as it stands, on the host cores, over whole decode steps of
+    the workload (all sequences of one batch) repeated for ~budget_s."""
+    nthreads = os.cpu_count() or 1
+    seqs = np.arange(nseq_batch)
+    lens = batch.context_lens[seqs]
+    elapsed, reps = 0.0, 0
+    while elapsed < budget_s or reps == 0:
+        elapsed += oracle_units_time(batch, seqs, nthreads)
+        reps += 1
+        if reps >= 1000:
+            break
+    kvb = kv_bytes(lens, batch.num_kv_heads, batch.head_dim, batch.elem_bytes) * reps
+    return {"value": kvb / elapsed / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{reps} full decode step(s) of the workload ({nseq_batch} sequences, fp64 C, "
+                      f"OpenMP over (sequence, KV head)), {elapsed:.1f} s",
+            "tokens_per_s": nseq_batch * reps / elapsed}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    batch, desc = build_workload(args.config, 0, 1)
+    nb = per_batch(args.config)
+    nthreads = os.cpu_count() or 1
+    # size each step's sample (whole sequences) so the K + W steps fit ~120 s
+    t1 = oracle_units_time(batch, np.arange(1), nthreads)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    per_step = int(max(1, min(nb, budget // max(t1, 1e-6))))
+    order = np.arange(nb)
+    for i in range(args.warmup):
+        oracle_units_time(batch, order[(i * per_step + np.arange(per_step)) % nb], nthreads)
+    total, kvb, seqs_done = 0.0, 0, 0
+    for i in range(args.steps):
+        seqs = order[(i * per_step + np.arange(per_step)) % nb]
+        total += oracle_units_time(batch, seqs, nthreads)
+        kvb += kv_bytes(batch.context_lens[seqs], batch.num_kv_heads, batch.head_dim, batch.elem_bytes)
+        seqs_done += len(seqs)
+    value = kvb / total / 1e9
+    line = {
+        "metric": "paged decode attention KV GB/s (Qwen3-8B shape)", "value": value, "unit": "GB/s",
+        "impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": {"workload": desc, "sample_seqs_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"{per_step} sequence(s) of the batch per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "tokens_per_s": seqs_done / total,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_121_gb300 as pa
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    pa.load_library()
+
+    copies = 2
+    batch, desc = build_workload(args.config, rank, copies)
+    nb = per_batch(args.config)
+    hq, hkv, d, bs = batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size
+    elem = batch.elem_bytes
+
+    def dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    k_cache, v_cache = dev(batch.k_cache), dev(batch.v_cache)
+    seq_all = np.arange(batch.num_seqs, dtype=np.int32)
+    slots_all = pa.pa_compute_slot_mapping(batch.block_tables, seq_all, batch.new_pos, bs)
+    views = []
+    for c in range(copies):
+        sl = slice(c * nb, (c + 1) * nb)
+        lens = batch.context_lens[sl]
+        views.append({
+            "query": dev(batch.query[sl]), "tables": dev(batch.block_tables[sl]),
+            "lens": dev(lens), "key": dev(batch.new_key[sl]), "value": dev(batch.new_value[sl]),
+            "slots": torch.from_numpy(slots_all[sl].copy()).cuda(),
+            "max_len": int(lens.max()), "lens_h": lens,
+            "out": torch.empty((nb, hq, d), dtype=torch.float32, device="cuda"),
+        })
+    ws_bytes = max(pa.pa_decode_workspace_size(nb, hq, hkv, d, bs, v["max_len"]) for v in views)
+    workspace = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+
+    def scatter(v):
+        pa.pa_reshape_and_cache(v["key"], v["value"], k_cache, v_cache, v["slots"])
+
+    def decode(v):
+        pa.pa_decode(v["out"], v["query"], k_cache, v_cache, v["tables"], v["lens"], v["max_len"],
+                     batch.scale, workspace=workspace)
+
+    def step(i):
+        v = views[i % copies]
+        scatter(v)
+        decode(v)
+
+    # correctness of the timed configuration against the oracle (one sequence sample)
+    for i in range(copies):
+        step(i)
+    torch.cuda.synchronize()
+    if pa.pa_device_status() != 0:
+        raise SystemExit("device status not clean after warm-up")
+
+    # CUDA graphs: one graph per batch view, each holding one whole step
+    stream = torch.cuda.Stream()
+    step_graphs, decode_graphs = [], []
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+        torch.cuda.synchronize()
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                step(c)
+            step_graphs.append(g)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                decode(views[c])
+            decode_graphs.append(g)
+    torch.cuda.synchronize()
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step_graphs[i % copies].replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_id_for_smi(torch, local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(K):
+            step_graphs[i % copies].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
+    steps_timed = K
+
+    # the dominant kernel alone: decode-only graph replays, CUDA events on its stream
+    dreps = max(100, min(K, 20000))
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            decode_graphs[c].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(dreps):
+            decode_graphs[i % copies].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    decode_ms = e0.elapsed_time(e1) / dreps
+
+    # e2e through the public API, host buffers (pinned), copies inside the timed region
+    h_in = []
+    for c in range(copies):
+        sl = slice(c * nb, (c + 1) * nb)
+        h_in.append({
+            "query": torch.from_numpy(batch.query[sl].view(np.int16).copy()).pin_memory(),
+            "tables": torch.from_numpy(batch.block_tables[sl].copy()).pin_memory(),
+            "lens": torch.from_numpy(batch.context_lens[sl].copy()).pin_memory(),
+            "key": torch.from_numpy(batch.new_key[sl].view(np.int16).copy()).pin_memory(),
+            "value": torch.from_numpy(batch.new_value[sl].view(np.int16).copy()).pin_memory(),
+            "slots": torch.from_numpy(slots_all[sl].copy()).pin_memory(),
+            "out": torch.empty((nb, hq, d), dtype=torch.float32).pin_memory(),
+        })
+    h2d = sum(h_in[0][k].numel() * h_in[0][k].element_size()
+              for k in ("query", "tables", "lens", "key", "value", "slots"))
+    d2h = h_in[0]["out"].numel() * 4
+    dq = torch.empty((nb, hq, d), dtype=torch.bfloat16, device="cuda")
+    dk = torch.empty((nb, hkv, d), dtype=torch.bfloat16, device="cuda")
+    dvv = torch.empty_like(dk)
+    dt = torch.empty_like(views[0]["tables"])
+    dl = torch.empty_like(views[0]["lens"])
+    ds = torch.empty_like(views[0]["slots"])
+    dout = torch.empty((nb, hq, d), dtype=torch.float32, device="cuda")
+
+    def e2e_step(i):
+        h = h_in[i % copies]
+        v = views[i % copies]
+        dq.view(torch.int16).copy_(h["query"], non_blocking=True)
+        dk.view(torch.int16).copy_(h["key"], non_blocking=True)
+        dvv.view(torch.int16).copy_(h["value"], non_blocking=True)
+        dt.copy_(h["tables"], non_blocking=True)
+        dl.copy_(h["lens"], non_blocking=True)
+        ds.copy_(h["slots"], non_blocking=True)
+        pa.pa_reshape_and_cache(dk, dvv, k_cache, v_cache, ds)
+        pa.pa_decode(dout, dq, k_cache, v_cache, dt, dl, v["max_len"], batch.scale, workspace=workspace)
+        h["out"].copy_(dout, non_blocking=True)
+        torch.cuda.current_stream().synchronize()   # the result is read on the host
+        return float(h["out"][0, 0, 0])
+
+    e2e_steps = min(K, 2000)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e2e_s = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    if pa.pa_device_status() != 0:
+        raise SystemExit("device status not clean after the timed region")
+
+    # max over ranks
+    ms_step = ms_total / steps_timed
+    e2e_ms_step = e2e_s * 1e3 / e2e_steps
+    if world > 1:
+        t = torch.tensor([ms_step, e2e_ms_step, decode_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms_step, decode_ms = (float(x) for x in t.tolist())
+
+    lens0 = views[0]["lens_h"]
+    step_kv = kv_bytes(lens0, hkv, d, elem)          # per batch; both batches have equal totals for qwen3/long
+    avg_kv = np.mean([kv_bytes(v["lens_h"], hkv, d, elem) for v in views])
+    value = world * avg_kv / (ms_step * 1e-3) / 1e9
+    e2e_value = world * avg_kv / (e2e_ms_step * 1e-3) / 1e9
+    alg = np.mean([decode_alg_bytes(v["lens_h"], hq, hkv, d, bs, elem) for v in views])
+    achieved = alg / (decode_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = profiled_traffic(args.config)
+    line = {
+        "metric": "paged decode attention KV GB/s (Qwen3-8B shape)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps_timed, "warmup": W,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), bf16-rounded; block placement a seeded random permutation)",
+        "config": {"workload": desc, "graphs": "one CUDA graph per step, %d batches alternate" % copies,
+                   "l2": "inputs larger than L2: 2 batches of %.0f MB alternate" % (step_kv / 1e6),
+                   "step": "reshape_and_cache(%d tokens) + pa_decode (fused split-K + LSE merge)" % nb},
+        "tokens_per_s": world * nb / (ms_step * 1e-3),
+        "pct_of_8tbs": 100.0 * value / HBM_NOMINAL_GBS,
+        "pct_of_measured_hbm": 100.0 * value / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "decode_mma_kernel<128,%d>" % bs, "peak_kind": peak_kind,
+                     "decode_us": decode_ms * 1e3, "alg_bytes_per_launch": int(alg)},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms_step, "steps": e2e_steps},
+        "gpu_launches": 2 * steps_timed,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(batch, nb, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=["qwen3", "long", "gqa"], default="qwen3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

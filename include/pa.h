@@ -1,0 +1,272 @@
+/*
+ * pa.h -- C ABI of libpa, the paged KV-cache hot path for NVIDIA GB300 (sm_103a).
+ *
+ * Device entry points enqueue work on the caller's CUDA stream and return as
+ * soon as the work is queued. They never allocate device memory, never
+ * synchronise, and check their host arguments before any launch: a call that
+ * returns anything but PA_OK has enqueued nothing. Faults inside a kernel
+ * surface at the caller's next synchronisation, as usual in CUDA.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named *_cache, query, key, value, out, block_tables,
+ *    context_lens, slot_mapping, block_mapping, tmp_out, max_logits,
+ *    exp_sums and workspace are caller-owned DEVICE memory, contiguous,
+ *    row-major, 16-byte aligned. The library keeps no reference after the
+ *    call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream), so that this header needs no CUDA include.
+ *  - KV cache layout: k_cache and v_cache are [num_blocks, block_size,
+ *    num_kv_heads, head_dim]; slot s = block * block_size + offset addresses
+ *    row s of the cache viewed as [num_blocks * block_size, num_kv_heads,
+ *    head_dim].
+ *  - Block tables: [num_seqs, max_blocks_per_seq] int32; entry j of row b is
+ *    the physical block that holds tokens [j*block_size, (j+1)*block_size) of
+ *    sequence b. Entries at or past cdiv(context_lens[b], block_size) are
+ *    never read.
+ *
+ * The source pages this follows are cited by title and section:
+ *  [P1] "PagedAttention: KV cache virtual memory" (news.ainew.jp, Arc 6)
+ *  [P3] "PagedAttention, explained." (vibeengines.com)
+ *  [P4] "What Does PagedAttention Actually Optimize?" (hrletsgo.me)
+ *  [P5] "Paged Attention: Virtual Memory for the KV Cache" (theservingstack.com)
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shapes */
+    PA_ERR_UNSUPPORTED = 2,   /* a shape / dtype combination no kernel handles */
+    PA_ERR_OUT_OF_BLOCKS = 3, /* block manager: the free list cannot satisfy the request */
+    PA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than pa_decode_workspace_size() */
+    PA_ERR_TIMEOUT = 5,       /* a kernel gave up waiting on an async copy (see pa_device_status) */
+    PA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch or attribute error) */
+    PA_ERR_NOT_FOUND = 7      /* block manager: unknown sequence id */
+} pa_status;
+
+typedef enum pa_dtype {
+    PA_F32 = 0,
+    PA_BF16 = 1
+} pa_dtype;
+
+/* Human-readable text of a status code (static storage, never NULL). */
+PA_API const char *pa_status_string(pa_status status);
+
+/* ABI version of this header (increases on any incompatible change). */
+#define PA_ABI_VERSION 1
+PA_API int pa_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * Slot scatter ("reshape_and_cache").
+ * [P3] procedure step 4 (each generated token's key and value go into the
+ * next free slot of the sequence's last block) and "Across GPUs" (fused
+ * kernels that write new keys and values into blocks); [P5] "Finding a
+ * token: position, block, slot" (slot = block number * block size + offset).
+ *
+ *   key, value    [num_tokens, num_kv_heads, head_dim], dtype kv_dtype
+ *   slot_mapping  [num_tokens] int64; token i is written to slot
+ *                 slot_mapping[i] of both caches (all heads, all dims).
+ *                 A negative slot skips the token (padding). A slot at or
+ *                 past num_blocks * block_size is skipped too (never written).
+ *   Distinct tokens must map to distinct slots; if two share a slot, which
+ *   one lands is unspecified.
+ *   Requires (num_kv_heads * head_dim * element size) % 16 == 0.
+ *   num_tokens == 0 is a no-op returning PA_OK.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                      void *v_cache, const int64_t *slot_mapping, int num_tokens,
+                                      int num_blocks, int block_size, int num_kv_heads,
+                                      int head_dim, pa_dtype kv_dtype, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Copy-on-write block copy ("copy_blocks").
+ * [P1] "Copy-on-write: when two requests share a prefix" (clone the one block
+ * being written); [P3] procedure step 6 and "Across GPUs" (the block copies
+ * copy-on-write needs).
+ *
+ *   block_mapping [num_pairs, 2] int64 (src, dst): block dst of k_cache and of
+ *                 v_cache becomes a byte copy of block src.
+ *   Preconditions: dst ids distinct and disjoint from src ids (otherwise
+ *   the result depends on copy order). Pairs with an id outside
+ *   [0, num_blocks) are skipped. num_pairs == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                                int num_pairs, int num_blocks, int block_size, int num_kv_heads,
+                                int head_dim, pa_dtype kv_dtype, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Paged single-query (decode) attention.
+ * [P4] section 8 (Attention(Q,K,V) = softmax(QK^T / sqrt(d)) V, unchanged by
+ * paging) and section 14 (per step: read the block table, find each
+ * position's logical block, translate to the physical block, add the
+ * offset, read K and V, compute scores and the weighted sum); [P3] step 5
+ * (fetch key and value blocks wherever the table says, block by block).
+ * Grouped-query attention: query head h reads KV head h / (num_heads /
+ * num_kv_heads) ([P3], legend of the KV-size formula).
+ *
+ *   out          [num_seqs, num_heads, head_dim], out_dtype (F32 or BF16)
+ *   query        [num_seqs, num_heads, head_dim], q_dtype
+ *   context_lens [num_seqs] int32: tokens attended by each sequence (the
+ *                token written this step included). 0 gives an all-zero row.
+ *   max_context_len  host-side upper bound of context_lens (sizes the grid;
+ *                tokens past it are not attended).
+ *   scale        multiplies q.k (normally 1/sqrt(head_dim)).
+ *   workspace    scratch for the context split: NULL / 0 bytes runs one
+ *                CTA per (sequence, KV head); otherwise at least
+ *                pa_decode_workspace_size() bytes, ZERO-FILLED before the
+ *                first call. The kernel leaves it ready for the next call
+ *                (its counters return to zero). Calls that share a
+ *                workspace must not overlap on the GPU.
+ *   Supported: head_dim 64 or 128; num_heads % num_kv_heads == 0;
+ *   (q, kv) dtypes (F32, F32) or (BF16, BF16); block_size 1..256.
+ *   bf16 caches with block_size 8, 16 or 32 run the tensor-core kernel.
+ * ---------------------------------------------------------------------- */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int max_context_len);
+
+PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
+                           const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                           int block_size, int max_blocks_per_seq, int num_blocks,
+                           int max_context_len, float scale, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Split-K decode: attention over fixed partitions of partition_size tokens
+ * (a multiple of block_size), to be combined by pa_lse_merge. The pages
+ * describe no split; its definition is the plain one: partition p of
+ * sequence b is softmax attention over tokens [p*partition_size,
+ * min(len, (p+1)*partition_size)), and long contexts still cost reads of
+ * every token ([P4] section 15).
+ *
+ *   tmp_out    [num_seqs, num_heads, max_partitions, head_dim] f32: the
+ *              partition's normalised output
+ *   max_logits [num_seqs, num_heads, max_partitions] f32: max of scale*q.k
+ *   exp_sums   [num_seqs, num_heads, max_partitions] f32: sum of exp(s - max)
+ *   with max_partitions = cdiv(max_context_len, partition_size). Partitions
+ *   past a sequence's length are written as (0, -inf, 0).
+ *   Other arguments as pa_decode.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_decode_splitk(float *tmp_out, float *max_logits, float *exp_sums,
+                                  int partition_size, const void *query, pa_dtype q_dtype,
+                                  const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_blocks_per_seq, int num_blocks,
+                                  int max_context_len, float scale, void *stream);
+
+/* Log-sum-exp merge of pa_decode_splitk's partitions:
+ *   M = max_p max_logits[p],  w_p = exp_sums[p] * exp(max_logits[p] - M),
+ *   out = sum_p w_p * tmp_out[p] / sum_p w_p   (0 if every w_p is 0).
+ * Only partitions p < cdiv(context_lens[b], partition_size) are read. */
+PA_API pa_status pa_lse_merge(void *out, pa_dtype out_dtype, const float *tmp_out,
+                              const float *max_logits, const float *exp_sums,
+                              const int32_t *context_lens, int num_seqs, int num_heads,
+                              int head_dim, int max_partitions, int partition_size,
+                              void *stream);
+
+/* Device status word: the kernels never spin without a bound. A wait on an
+ * asynchronous copy that exceeds its time limit makes the kernel record
+ * PA_ERR_TIMEOUT here, drain its own copies and return. This call copies the
+ * word to *status (after synchronising `stream`) and, if `clear`, resets it.
+ * One word per device, shared by every call on that device. */
+PA_API pa_status pa_device_status(int *status, int clear, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host slot map: slot_mapping[i] = block_tables[seq[i]][pos[i] / block_size]
+ *                 * block_size + pos[i] % block_size   (pos[i] < 0 gives -1)
+ * [P5] "Finding a token: position, block, slot"; [P4] section 17 (write_kv).
+ * All pointers are HOST memory here. Returns PA_ERR_INVALID_ARG if a position
+ * falls past max_blocks_per_seq blocks or a sequence index is out of range.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_compute_slot_mapping(int64_t *slot_mapping, const int32_t *block_tables,
+                                         int num_seqs, int max_blocks_per_seq,
+                                         const int32_t *seq_index, const int32_t *positions,
+                                         int num_tokens, int block_size);
+
+/* ------------------------------------------------------------------------
+ * Host block manager (plain C++, host memory only).
+ * [P5] "Paging: blocks handed out as tokens arrive" and "Inside vLLM: the
+ * block pool": a pool of fixed-size blocks, a free queue (allocation pops the
+ * front), cdiv(num_tokens, block_size) blocks for a prompt, one more block
+ * each time the last fills, block 0 reserved as the null block, freed blocks
+ * returned to the queue front. [P3] procedure steps 1-4 and 6 and [P1]
+ * "Copy-on-write": reference counts; a write into a block whose count is
+ * above one first clones it (the caller copies the data with
+ * pa_copy_blocks), drops the original's count and repoints only the
+ * writer's table.
+ * Not thread-safe: one handle per thread, or external locking.
+ * Sequence ids are arbitrary int64 values chosen by the caller.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_bm pa_bm;
+
+typedef struct pa_bm_stats_t {
+    int64_t num_blocks;     /* usable blocks (the null block excluded) */
+    int64_t free_blocks;    /* blocks on the free queue */
+    int64_t used_blocks;    /* physical blocks with refcount >= 1 */
+    int64_t shared_blocks;  /* physical blocks with refcount >= 2 */
+    int64_t num_seqs;
+    int64_t logical_blocks; /* sum over sequences of their table lengths */
+    int64_t num_tokens;     /* sum over sequences of their token counts */
+    int64_t waste_slots;    /* logical_blocks * block_size - num_tokens */
+    int64_t cow_copies;     /* copy-on-write clones made so far */
+} pa_bm_stats_t;
+
+/* reserve_null_block != 0 keeps block 0 out of the free queue. The free
+ * queue starts in ascending id order. */
+PA_API pa_status pa_bm_create(int num_blocks, int block_size, int reserve_null_block,
+                              pa_bm **out);
+/* As pa_bm_create, with the free queue given explicitly (front first):
+ * `free_order` lists n distinct ids in [0, num_blocks). */
+PA_API pa_status pa_bm_create_with_free_list(int num_blocks, int block_size,
+                                             const int32_t *free_order, int n, pa_bm **out);
+PA_API void pa_bm_destroy(pa_bm *bm);
+
+/* New sequence holding num_tokens tokens: takes cdiv(num_tokens, block_size)
+ * blocks (refcount 1). PA_ERR_OUT_OF_BLOCKS leaves the manager unchanged;
+ * PA_ERR_INVALID_ARG if `seq` already exists. */
+PA_API pa_status pa_bm_allocate(pa_bm *bm, int64_t seq, int num_tokens);
+
+/* Room for one more token of `seq`. Writes its slot id, and -1/-1 to
+ * cow_src/cow_dst, or the (src, dst) pair to copy before writing when the
+ * token falls in a shared block. A full last block takes a fresh block.
+ * PA_ERR_OUT_OF_BLOCKS leaves the manager unchanged. */
+PA_API pa_status pa_bm_append_slot(pa_bm *bm, int64_t seq, int64_t *slot, int64_t *cow_src,
+                                   int64_t *cow_dst);
+
+/* `child` starts as a copy of `parent`: same table and token count, one more
+ * reference on each block. */
+PA_API pa_status pa_bm_fork(pa_bm *bm, int64_t parent, int64_t child);
+
+/* Drops one reference on each of the sequence's blocks; blocks reaching zero
+ * return to the front of the free queue, in block-table order. */
+PA_API pa_status pa_bm_free(pa_bm *bm, int64_t seq);
+
+/* Copies the sequence's table into out[0..cap) and its length into *n
+ * (PA_ERR_INVALID_ARG if cap < *n; *n is still set). */
+PA_API pa_status pa_bm_block_table(const pa_bm *bm, int64_t seq, int32_t *out, int cap, int *n);
+PA_API pa_status pa_bm_num_tokens(const pa_bm *bm, int64_t seq, int *n);
+PA_API pa_status pa_bm_refcount(const pa_bm *bm, int block, int *refcount);
+PA_API pa_status pa_bm_stats(const pa_bm *bm, pa_bm_stats_t *out);
+/* Free queue, front first (same cap / n convention as pa_bm_block_table). */
+PA_API pa_status pa_bm_free_list(const pa_bm *bm, int32_t *out, int cap, int *n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

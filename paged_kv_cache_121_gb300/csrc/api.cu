@@ -1,0 +1,417 @@
+// C ABI of libpa: argument checks, work planning, TMA descriptors, launches.
+// Declarations and the contract of each entry point are in include/pa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/pa.h"
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace pa {
+
+// Device status word (one per device that loads the library): kernels record
+// a bounded-wait timeout here; read and cleared through pa_device_status.
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kCtasPerSm = 2;         // resident decode CTAs per SM the split plan aims at
+constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
+
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int *> g_status_addr[kMaxDevices];
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int element_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+
+bool valid_dtype(pa_dtype t) { return t == PA_F32 || t == PA_BF16; }
+
+pa_status current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (*dev < 0 || *dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+int sm_count(int dev) {
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 0;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int *status_word(int dev) {
+    int *p = g_status_addr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return nullptr;
+    g_status_addr[dev].store(static_cast<int *>(addr), std::memory_order_release);
+    return static_cast<int *>(addr);
+}
+
+// Optional tuning knob read once: resident CTAs per SM assumed by the split plan.
+int ctas_per_sm_target() {
+    static const int v = [] {
+        const char *e = std::getenv("PA_DECODE_CTAS_PER_SM");
+        const int x = e ? std::atoi(e) : 0;
+        return (x >= 1 && x <= 64) ? x : kCtasPerSm;
+    }();
+    return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// 4-D view of a bf16 cache [num_blocks, block_size, Hkv, D] (innermost first:
+// D, Hkv, block_size, num_blocks); box = 64 dims x 1 head x block_size tokens
+// x 1 block, 128-byte swizzle. Out-of-range block ids read as zeros.
+pa_status make_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int block_size,
+                         int num_kv_heads, int head_dim) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return PA_ERR_CUDA;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
+                                static_cast<cuuint64_t>(block_size), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
+    const cuuint64_t strides[3] = {row, row * num_kv_heads, row * num_kv_heads * block_size};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(block_size), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+struct DecodeShape {
+    int num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks, num_blocks, max_ctx;
+};
+
+pa_status check_shape(const DecodeShape &s) {
+    if (s.num_seqs < 0 || s.num_heads <= 0 || s.num_kv_heads <= 0 || s.max_blocks <= 0 ||
+        s.num_blocks <= 0 || s.max_ctx < 0 || s.block_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (s.num_heads % s.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(s.max_ctx) > static_cast<int64_t>(s.max_blocks) * s.block_size)
+        return PA_ERR_INVALID_ARG;
+    if (s.head_dim != 64 && s.head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (s.block_size > 256) return PA_ERR_UNSUPPORTED;
+    const int ntile = (s.num_heads / s.num_kv_heads + kRowsPerTile - 1) / kRowsPerTile;
+    if (s.num_seqs > 65535 || static_cast<int64_t>(s.num_kv_heads) * ntile > 65535)
+        return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+struct Plan {
+    int ntile;
+    int nsplit;
+    int part_blocks;
+};
+
+// Split each (sequence, KV head, head tile) context so that about
+// sm_count * ctas_per_sm CTAs exist, with at least kMinSplitTokens per piece.
+Plan plan_split(const DecodeShape &s, int sms) {
+    Plan pl;
+    const int group = s.num_heads / s.num_kv_heads;
+    pl.ntile = (group + kRowsPerTile - 1) / kRowsPerTile;
+    const int64_t units = static_cast<int64_t>(s.num_seqs) * s.num_kv_heads * pl.ntile;
+    const int64_t nblk = std::max<int64_t>(1, cdiv64(s.max_ctx, s.block_size));
+    const int64_t cap = static_cast<int64_t>(sms) * ctas_per_sm_target();
+    int64_t nsplit = 1;
+    if (units > 0 && units < cap) {
+        nsplit = cap / units;
+        const int64_t min_pb = std::max<int64_t>(1, cdiv64(kMinSplitTokens, s.block_size));
+        nsplit = std::min(nsplit, std::max<int64_t>(1, nblk / min_pb));
+        nsplit = std::min<int64_t>(nsplit, kMaxSplits);
+    }
+    const int64_t pb = cdiv64(nblk, nsplit);
+    pl.part_blocks = static_cast<int>(pb);
+    pl.nsplit = static_cast<int>(cdiv64(nblk, pb));
+    return pl;
+}
+
+struct WorkspaceLayout {
+    size_t o_off, ml_off, count_off, total;
+};
+
+WorkspaceLayout workspace_layout(const DecodeShape &s, const Plan &pl) {
+    WorkspaceLayout w{};
+    if (pl.nsplit <= 1) return w;
+    const size_t rows = static_cast<size_t>(s.num_seqs) * s.num_heads * pl.nsplit;
+    w.o_off = 0;
+    w.ml_off = align256(rows * s.head_dim * sizeof(float));
+    w.count_off = w.ml_off + align256(rows * 2 * sizeof(float));
+    w.total = w.count_off +
+              align256(static_cast<size_t>(s.num_seqs) * s.num_kv_heads * pl.ntile * sizeof(unsigned));
+    return w;
+}
+
+pa_status check_dtypes(pa_dtype q_dtype, pa_dtype kv_dtype) {
+    if (!valid_dtype(q_dtype) || !valid_dtype(kv_dtype)) return PA_ERR_INVALID_ARG;
+    if (q_dtype != kv_dtype) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// Shared by pa_decode and pa_decode_splitk.
+pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, int dev,
+                        cudaStream_t stream) {
+    const bool bf16 = kv_dtype == PA_BF16;
+    p.status = status_word(dev);
+    if (!p.status) return PA_ERR_CUDA;
+    const dim3 grid(static_cast<unsigned>(p.nsplit),
+                    static_cast<unsigned>(s.num_kv_heads * p.ntile), static_cast<unsigned>(s.num_seqs));
+    cudaError_t e;
+    if (bf16 && decode_mma_supported(s.head_dim, s.block_size)) {
+        CUtensorMap tk, tv;
+        pa_status st = make_cache_map(&tk, p.k_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim);
+        if (st != PA_OK) return st;
+        st = make_cache_map(&tv, p.v_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim);
+        if (st != PA_OK) return st;
+        e = launch_decode_mma(p, tk, tv, grid, stream);
+    } else {
+        e = launch_decode_simt(p, bf16, grid, stream);
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+void fill_common(DecodeParams &p, const DecodeShape &s, const void *query, pa_dtype q_dtype,
+                 const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                 const int32_t *context_lens, float scale) {
+    std::memset(&p, 0, sizeof p);
+    p.query = query;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.num_seqs = s.num_seqs;
+    p.num_heads = s.num_heads;
+    p.num_kv_heads = s.num_kv_heads;
+    p.head_dim = s.head_dim;
+    p.block_size = s.block_size;
+    p.max_blocks = s.max_blocks;
+    p.num_blocks = s.num_blocks;
+    p.group = s.num_heads / s.num_kv_heads;
+    p.q_bf16 = q_dtype == PA_BF16;
+    p.scale_log2 = scale * kLog2e;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+PA_API const char *pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_OUT_OF_BLOCKS: return "out of KV blocks";
+        case PA_ERR_WORKSPACE: return "workspace missing or too small";
+        case PA_ERR_TIMEOUT: return "kernel wait timed out";
+        case PA_ERR_CUDA: return "CUDA runtime error";
+        case PA_ERR_NOT_FOUND: return "unknown sequence";
+    }
+    return "unknown status";
+}
+
+PA_API int pa_abi_version(void) { return PA_ABI_VERSION; }
+
+PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                      void *v_cache, const int64_t *slot_mapping, int num_tokens,
+                                      int num_blocks, int block_size, int num_kv_heads,
+                                      int head_dim, pa_dtype kv_dtype, void *stream) {
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        !valid_dtype(kv_dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * element_bytes(kv_dtype);
+    if (row_bytes % 16 != 0 || row_bytes / 16 > (1 << 20)) return PA_ERR_UNSUPPORTED;
+    const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
+    cudaError_t e = launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                             num_slots, static_cast<int>(row_bytes), as_stream(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                                int num_pairs, int num_blocks, int block_size, int num_kv_heads,
+                                int head_dim, pa_dtype kv_dtype, void *stream) {
+    if (num_pairs < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        !valid_dtype(kv_dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_cache || !v_cache || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes =
+        static_cast<int64_t>(block_size) * num_kv_heads * head_dim * element_bytes(kv_dtype);
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    cudaError_t e = launch_copy_blocks(k_cache, v_cache, block_mapping, num_pairs, num_blocks,
+                                       block_bytes, as_stream(stream));
+    if (e == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int max_context_len) {
+    const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        std::max(1, block_size > 0 ? (max_context_len + block_size - 1) / block_size : 1),
+                        1, max_context_len};
+    if (check_shape(s) != PA_OK) return 0;
+    int dev;
+    if (current_device(&dev) != PA_OK) return 0;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return 0;
+    return workspace_layout(s, plan_split(s, sms)).total;
+}
+
+PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
+                           const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                           int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           int max_blocks_per_seq, int num_blocks, int max_context_len, float scale,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        max_blocks_per_seq, num_blocks, max_context_len};
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    if (!valid_dtype(out_dtype) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    int dev;
+    if ((st = current_device(&dev)) != PA_OK) return st;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PA_ERR_CUDA;
+
+    Plan pl = plan_split(s, sms);
+    DecodeParams p;
+    fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
+    p.out = out;
+    p.out_bf16 = out_dtype == PA_BF16;
+    p.ntile = pl.ntile;
+    if (workspace == nullptr && workspace_bytes == 0) {
+        // no scratch: one CTA per (sequence, KV head, head tile)
+        pl.part_blocks = std::max(1, (max_context_len + block_size - 1) / block_size);
+        pl.nsplit = 1;
+    }
+    p.nsplit = pl.nsplit;
+    p.part_blocks = pl.part_blocks;
+    if (pl.nsplit > 1) {
+        const WorkspaceLayout wl = workspace_layout(s, pl);
+        if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+        char *ws = static_cast<char *>(workspace);
+        p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+        p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+        p.ws_count = reinterpret_cast<unsigned *>(ws + wl.count_off);
+        p.mode = kModeFused;
+    } else {
+        p.mode = kModeFinal;
+    }
+    return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
+}
+
+PA_API pa_status pa_decode_splitk(float *tmp_out, float *max_logits, float *exp_sums,
+                                  int partition_size, const void *query, pa_dtype q_dtype,
+                                  const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_blocks_per_seq, int num_blocks,
+                                  int max_context_len, float scale, void *stream) {
+    const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        max_blocks_per_seq, num_blocks, max_context_len};
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % block_size != 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
+    const int64_t P = cdiv64(max_context_len, partition_size);
+    if (num_seqs == 0 || P == 0) return PA_OK;
+    if (P > 65535) return PA_ERR_UNSUPPORTED;
+    if (!tmp_out || !max_logits || !exp_sums || !query || !k_cache || !v_cache || !block_tables ||
+        !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    int dev;
+    if ((st = current_device(&dev)) != PA_OK) return st;
+    DecodeParams p;
+    fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.ntile = (s.num_heads / s.num_kv_heads + kRowsPerTile - 1) / kRowsPerTile;
+    p.nsplit = static_cast<int>(P);
+    p.part_blocks = partition_size / block_size;
+    p.mode = kModeSplitK;
+    return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
+}
+
+PA_API pa_status pa_lse_merge(void *out, pa_dtype out_dtype, const float *tmp_out,
+                              const float *max_logits, const float *exp_sums,
+                              const int32_t *context_lens, int num_seqs, int num_heads,
+                              int head_dim, int max_partitions, int partition_size, void *stream) {
+    if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_partitions <= 0 || partition_size <= 0 ||
+        !valid_dtype(out_dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (num_seqs > 65535 || static_cast<size_t>(max_partitions) * sizeof(float) > 200 * 1024)
+        return PA_ERR_UNSUPPORTED;
+    if (!out || !tmp_out || !max_logits || !exp_sums || !context_lens) return PA_ERR_INVALID_ARG;
+    cudaError_t e = launch_lse_merge(out, out_dtype == PA_BF16, tmp_out, max_logits, exp_sums,
+                                     context_lens, num_seqs, num_heads, head_dim, max_partitions,
+                                     partition_size, as_stream(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_device_status(int *status, int clear, void *stream) {
+    if (!status) return PA_ERR_INVALID_ARG;
+    int dev;
+    pa_status st = current_device(&dev);
+    if (st != PA_OK) return st;
+    int *addr = status_word(dev);
+    if (!addr) return PA_ERR_CUDA;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(status, addr, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    if (clear && *status != 0) {
+        const int zero = 0;
+        if (cudaMemcpyAsync(addr, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// The two companion kernels of paged decode.
+//
+// reshape_and_cache: each new token's key and value rows (all KV heads) are
+// written into its slot of the block pool -- "PagedAttention, explained.",
+// procedure step 4 and "Across GPUs" (the fused write kernels); slot =
+// block * block_size + offset, "Paged Attention: Virtual Memory for the KV
+// Cache", section "Finding a token: position, block, slot". In the
+// [num_blocks, block_size, Hkv, D] layout a slot is one contiguous row of
+// Hkv * D elements, so the scatter is a row copy with 16-byte vectors.
+//
+// copy_blocks: copy-on-write clones whole blocks before a shared block is
+// written -- "PagedAttention: KV cache virtual memory", section
+// "Copy-on-write"; "How PagedAttention Eliminates KV-Cache Fragmentation",
+// section "Advanced Memory Sharing and Copy-on-Write". Each CTA copies one
+// 8 KiB chunk of one block of one cache with 16-byte vectors.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace pa {
+
+__global__ void __launch_bounds__(128)
+reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                         uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                         const int64_t *__restrict__ slot_mapping, int64_t num_slots, int row_vecs) {
+    const int i = blockIdx.x;
+    const int64_t slot = slot_mapping[i];
+    if (slot < 0 || slot >= num_slots) return;
+    const uint4 *ks = key + static_cast<int64_t>(i) * row_vecs;
+    const uint4 *vs = value + static_cast<int64_t>(i) * row_vecs;
+    uint4 *kd = k_cache + slot * row_vecs;
+    uint4 *vd = v_cache + slot * row_vecs;
+    for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
+        const uint4 a = ks[c];
+        const uint4 v = vs[c];
+        kd[c] = a;
+        vd[c] = v;
+    }
+}
+
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                     void *v_cache, const int64_t *slot_mapping, int num_tokens,
+                                     int64_t num_slots, int row_bytes, cudaStream_t stream) {
+    const int row_vecs = row_bytes / 16;
+    const int threads = row_vecs >= 128 ? 128 : ((row_vecs + 31) / 32) * 32;
+    reshape_and_cache_kernel<<<num_tokens, threads, 0, stream>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_slots,
+        row_vecs);
+    return cudaGetLastError();
+}
+
+constexpr int kCopyChunkVecs = 512;  // 8 KiB per CTA
+
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                   const int64_t *__restrict__ block_mapping, int64_t num_blocks,
+                   int64_t block_vecs) {
+    const int pair = blockIdx.x;
+    const int which = blockIdx.y & 1;
+    const int64_t chunk = blockIdx.y >> 1;
+    const int64_t src = block_mapping[2 * static_cast<int64_t>(pair)];
+    const int64_t dst = block_mapping[2 * static_cast<int64_t>(pair) + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return;
+    uint4 *base = which ? v_cache : k_cache;
+    const uint4 *s = base + src * block_vecs;
+    uint4 *d = base + dst * block_vecs;
+    const int64_t c0 = chunk * kCopyChunkVecs;
+    const int64_t c1 = c0 + kCopyChunkVecs < block_vecs ? c0 + kCopyChunkVecs : block_vecs;
+    for (int64_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) d[c] = s[c];
+}
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                               int num_pairs, int64_t num_blocks, int64_t block_bytes,
+                               cudaStream_t stream) {
+    const int64_t block_vecs = block_bytes / 16;
+    const int64_t chunks = (block_vecs + kCopyChunkVecs - 1) / kCopyChunkVecs;
+    if (chunks * 2 > 65535) return cudaErrorInvalidValue;
+    dim3 grid(num_pairs, static_cast<unsigned>(chunks * 2));
+    copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(k_cache),
+                                                 static_cast<uint4 *>(v_cache), block_mapping,
+                                                 num_blocks, block_vecs);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,240 @@
+// Paged decode attention on the CUDA cores (fp32 caches, and bf16 caches
+// whose block size the tensor-core kernel does not take), plus the
+// log-sum-exp merge of split-K partitions.
+//
+// Same work decomposition and epilogue as the tensor-core kernel: one CTA per
+// (sequence, KV head, head tile, partition). Each warp takes every fourth
+// token of the partition; a lane owns head_dim/32 consecutive dims (one
+// coalesced vector load per K or V row), dot products are reduced with warp
+// shuffles, and the online softmax runs in fp32 in base 2.
+// Pages: "What Does PagedAttention Actually Optimize?", sections 8, 14 and
+// 17 (read_kv: logical block = t / B, offset = t % B, physical block from the
+// table).
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace pa {
+
+template <int E, typename KV>
+struct RowLoad;
+
+template <int E>
+struct RowLoad<E, float> {
+    __device__ static void load(const float *row, float (&x)[E]) {
+        if constexpr (E == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(row);
+            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+        } else if constexpr (E == 2) {
+            const float2 v = *reinterpret_cast<const float2 *>(row);
+            x[0] = v.x; x[1] = v.y;
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[e] = row[e];
+        }
+    }
+};
+
+template <int E>
+struct RowLoad<E, __nv_bfloat16> {
+    __device__ static void load(const __nv_bfloat16 *row, float (&x)[E]) {
+        if constexpr (E == 4) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(row);
+            x[0] = bf16_bits_to_float(v.x & 0xffffu); x[1] = bf16_bits_to_float(v.x >> 16);
+            x[2] = bf16_bits_to_float(v.y & 0xffffu); x[3] = bf16_bits_to_float(v.y >> 16);
+        } else if constexpr (E == 2) {
+            const uint32_t v = *reinterpret_cast<const uint32_t *>(row);
+            x[0] = bf16_bits_to_float(v & 0xffffu); x[1] = bf16_bits_to_float(v >> 16);
+        } else {
+            const uint16_t *u = reinterpret_cast<const uint16_t *>(row);
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[e] = bf16_bits_to_float(u[e]);
+        }
+    }
+};
+
+template <int D, int MAXR, typename KV>
+__global__ void __launch_bounds__(128)
+decode_simt_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int E = D / 32;
+    constexpr int kWarps = 4;
+    extern __shared__ float smem_f[];
+
+    const int part = blockIdx.x;
+    const int g = blockIdx.y / p.ntile;
+    const int tile = blockIdx.y % p.ntile;
+    const int b = blockIdx.z;
+    const int rows = min(kRowsPerTile, p.group - tile * kRowsPerTile);
+    const SeqWork w = seq_work(p, b, part);
+    if (w.blk_begin >= w.blk_end) {
+        write_empty<D>(p, b, g, tile, part, rows, w.nparts);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h0 = g * p.group + tile * kRowsPerTile;
+
+    float q[MAXR][E], o[MAXR][E], m[MAXR], l[MAXR];
+#pragma unroll
+    for (int r = 0; r < MAXR; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[r][e] = q[r][e] = 0.f;
+        if (r < rows) {
+            const int64_t off = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + lane * E;
+            if (p.q_bf16)
+                RowLoad<E, __nv_bfloat16>::load(static_cast<const __nv_bfloat16 *>(p.query) + off, q[r]);
+            else
+                RowLoad<E, float>::load(static_cast<const float *>(p.query) + off, q[r]);
+        }
+    }
+
+    const KV *kc = static_cast<const KV *>(p.k_cache);
+    const KV *vc = static_cast<const KV *>(p.v_cache);
+    const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+    const int t_begin = w.blk_begin * p.block_size;
+    const int t_end = min(w.len, w.blk_end * p.block_size);
+    for (int t = t_begin + warp; t < t_end; t += kWarps) {
+        const int64_t phys = table[t / p.block_size];
+        float kx[E], vx[E];
+        if (phys >= 0 && phys < p.num_blocks) {
+            const int64_t row = ((phys * p.block_size + t % p.block_size) * p.num_kv_heads + g) * D + lane * E;
+            RowLoad<E, KV>::load(kc + row, kx);
+            RowLoad<E, KV>::load(vc + row, vx);
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) kx[e] = vx[e] = 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < MAXR; ++r) {
+            if (r >= rows) break;
+            float s = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) s = fmaf(q[r][e], kx[e], s);
+#pragma unroll
+            for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            s *= p.scale_log2;
+            const float mn = fmaxf(m[r], s);
+            const float a = fast_exp2(m[r] - mn);
+            const float pr = fast_exp2(s - mn);
+            l[r] = l[r] * a + pr;
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[r][e] = fmaf(o[r][e], a, pr * vx[e]);
+            m[r] = mn;
+        }
+    }
+
+    using L = MergeLayout<D>;
+#pragma unroll
+    for (int r = 0; r < kRowsPerTile; ++r) {
+        if (r < MAXR) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) L::o(smem_f, warp)[r * L::kStride + lane * E + e] = o[r][e];
+            if (lane == 0) {
+                L::m(smem_f, warp)[r] = m[r];
+                L::l(smem_f, warp)[r] = l[r];
+            }
+        } else if (lane == 0) {
+            L::m(smem_f, warp)[r] = -INFINITY;
+            L::l(smem_f, warp)[r] = 0.f;
+        }
+    }
+    __syncthreads();
+    combine_warps<D>(smem_f, kWarps, rows);
+    write_result<D>(p, smem_f, kWarps, b, g, tile, part, rows, w.nparts);
+}
+
+template <int D, int MAXR, typename KV>
+static cudaError_t launch_simt_impl(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
+    auto kern = decode_simt_kernel<D, MAXR, KV>;
+    const size_t smem = MergeLayout<D>::bytes(4);
+    cudaError_t e = ensure_smem_limit(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 128, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, typename KV>
+static cudaError_t launch_simt_rows(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
+    const int rows = p.group < kRowsPerTile ? p.group : kRowsPerTile;
+    if (rows <= 1) return launch_simt_impl<D, 1, KV>(p, grid, stream);
+    if (rows <= 2) return launch_simt_impl<D, 2, KV>(p, grid, stream);
+    if (rows <= 4) return launch_simt_impl<D, 4, KV>(p, grid, stream);
+    if (rows <= 8) return launch_simt_impl<D, 8, KV>(p, grid, stream);
+    return launch_simt_impl<D, 16, KV>(p, grid, stream);
+}
+
+cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, cudaStream_t stream) {
+    if (p.head_dim == 128)
+        return kv_bf16 ? launch_simt_rows<128, __nv_bfloat16>(p, grid, stream)
+                       : launch_simt_rows<128, float>(p, grid, stream);
+    if (p.head_dim == 64)
+        return kv_bf16 ? launch_simt_rows<64, __nv_bfloat16>(p, grid, stream)
+                       : launch_simt_rows<64, float>(p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// log-sum-exp merge of split-K partitions: one CTA per (head, sequence)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128)
+lse_merge_kernel(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
+                 const float *exp_sums, const int32_t *context_lens, int num_heads, int head_dim,
+                 int max_partitions, int partition_size) {
+    extern __shared__ float wgt[];  // [max_partitions]
+    __shared__ float s_inv;
+    const int h = blockIdx.x, b = blockIdx.y;
+    int len = context_lens[b];
+    if (len < 0) len = 0;
+    const int np = min((len + partition_size - 1) / partition_size, max_partitions);
+    const int64_t row0 = (static_cast<int64_t>(b) * num_heads + h) * max_partitions;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        float M = -INFINITY;
+        for (int q = lane; q < np; q += 32)
+            if (exp_sums[row0 + q] > 0.f) M = fmaxf(M, max_logits[row0 + q]);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float tot = 0.f;
+        for (int q = lane; q < np; q += 32) {
+            const float es = exp_sums[row0 + q];
+            const float wq = es > 0.f ? es * fast_exp2((max_logits[row0 + q] - M) * kLog2e) : 0.f;
+            wgt[q] = wq;
+            tot += wq;
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        if (lane == 0) s_inv = tot > 0.f ? 1.f / tot : 0.f;
+    }
+    __syncthreads();
+    const float inv = s_inv;
+    for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
+        float acc = 0.f;
+        for (int q = 0; q < np; ++q) {
+            const float wq = wgt[q];
+            if (wq != 0.f) acc += wq * tmp_out[(row0 + q) * head_dim + d];
+        }
+        const int64_t oi = (static_cast<int64_t>(b) * num_heads + h) * head_dim + d;
+        if (out_bf16)
+            reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(acc * inv);
+        else
+            reinterpret_cast<float *>(out)[oi] = acc * inv;
+    }
+}
+
+cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
+                             const float *exp_sums, const int32_t *context_lens, int num_seqs,
+                             int num_heads, int head_dim, int max_partitions, int partition_size,
+                             cudaStream_t stream) {
+    const size_t smem = sizeof(float) * static_cast<size_t>(max_partitions);
+    if (smem > 48 * 1024) {
+        cudaError_t e = ensure_smem_limit(lse_merge_kernel, 200 * 1024);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid(num_heads, num_seqs);
+    lse_merge_kernel<<<grid, 128, smem, stream>>>(out, out_bf16, tmp_out, max_logits, exp_sums,
+                                                  context_lens, num_heads, head_dim, max_partitions,
+                                                  partition_size);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

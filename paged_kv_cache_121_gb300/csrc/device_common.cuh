@@ -1,0 +1,401 @@
+// Device-side building blocks shared by the decode kernels: parameter block,
+// PTX wrappers (mbarrier, TMA, ldmatrix, mma), bounded waits, and the CTA
+// epilogue that either writes the final output, writes split-K partitions,
+// or merges partitions in the last CTA to finish (log-sum-exp).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kRowsPerTile = 16;     // query heads per CTA (the MMA's M)
+constexpr int kMaxSplits = 256;      // bound on fused partitions (merge weights live in smem)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far above any legal wait
+
+enum DecodeMode : int { kModeFinal = 0, kModeSplitK = 1, kModeFused = 2 };
+enum StatusCode : int { kStatusTimeout = 5 };
+
+// Everything a decode launch needs; passed by value.
+struct DecodeParams {
+    const void *query;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    void *out;
+    float *tmp_out;      // split-K mode
+    float *max_logits;
+    float *exp_sums;
+    float *ws_o;         // fused mode: [B, Hq, nsplit, D] unnormalised partials
+    float *ws_ml;        // fused mode: [B, Hq, nsplit, 2] (max in log2 units, sum)
+    unsigned *ws_count;  // fused mode: [B, Hkv, ntile] arrival counters (zero between calls)
+    int *status;         // device status word
+    int num_seqs, num_heads, num_kv_heads, head_dim, block_size;
+    int max_blocks, num_blocks;
+    int group;           // num_heads / num_kv_heads
+    int ntile;           // cdiv(group, 16)
+    int nsplit;          // grid.x: partitions per (sequence, head tile)
+    int part_blocks;     // blocks per partition
+    int mode;
+    int out_bf16;
+    int q_bf16;
+    float scale_log2;    // scale * log2(e): scores are kept in base-2 units
+};
+
+// Raise a kernel's dynamic shared-memory limit once per device (host side;
+// keeps the call out of CUDA-graph capture after the first launch).
+template <typename Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kern, size_t bytes) {
+    static unsigned long long done_mask = 0;  // bit d: device d configured
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess && bit) __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
+    return e;
+}
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void record_status(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier (shared::cta)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; gives up after
+// kWaitLimitNs and returns false (the caller records a timeout and unwinds).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA: 4-D tiled load global -> shared, completion counted on an mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+        "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---------------------------------------------------------------------------
+// warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                            uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                                  uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// Per-sequence bookkeeping shared by every decode kernel
+// ---------------------------------------------------------------------------
+struct SeqWork {
+    int len;        // tokens attended (clamped to the table's capacity)
+    int nblk;       // blocks holding those tokens
+    int nparts;     // partitions with work (fused / final modes)
+    int blk_begin;  // this CTA's first block
+    int blk_end;    // one past its last block
+};
+
+__device__ __forceinline__ SeqWork seq_work(const DecodeParams &p, int b, int part) {
+    SeqWork w;
+    int len = p.context_lens[b];
+    if (len < 0) len = 0;
+    const int cap = p.max_blocks * p.block_size;
+    if (len > cap) len = cap;
+    int nblk = (len + p.block_size - 1) / p.block_size;
+    int nparts = (nblk + p.part_blocks - 1) / p.part_blocks;
+    if (nparts > p.nsplit) {
+        nparts = p.nsplit;
+        nblk = nparts * p.part_blocks;
+        len = nblk * p.block_size;
+    }
+    w.len = len;
+    w.nblk = nblk;
+    w.nparts = nparts;
+    w.blk_begin = part * p.part_blocks;
+    w.blk_end = min(nblk, w.blk_begin + p.part_blocks);
+    return w;
+}
+
+// ---------------------------------------------------------------------------
+// CTA result: per-warp partial softmax states combined, then written out.
+//
+// Shared-memory layout (floats), row stride D + 4:
+//   warp region w: m[16], l[16], O[16][D+4]   for w < nwarps
+//   cta region:    m[16], l[16], O[16][D+4]
+//   merge weights: [16][kMaxSplits]
+// m is a running max of base-2 scores, l the sum of 2^(s - m), O the
+// unnormalised sum of 2^(s - m) * v.
+// ---------------------------------------------------------------------------
+template <int D>
+struct MergeLayout {
+    static constexpr int kStride = D + 4;
+    static constexpr int kRegion = 32 + kRowsPerTile * kStride;
+    __device__ static float *m(float *base, int w) { return base + w * kRegion; }
+    __device__ static float *l(float *base, int w) { return base + w * kRegion + 16; }
+    __device__ static float *o(float *base, int w) { return base + w * kRegion + 32; }
+    static constexpr size_t bytes(int nwarps) {
+        return sizeof(float) * (static_cast<size_t>(nwarps + 1) * kRegion +
+                                static_cast<size_t>(kRowsPerTile) * kMaxSplits);
+    }
+};
+
+// Combine nwarps warp regions into the CTA region (all threads participate).
+template <int D>
+__device__ void combine_warps(float *base, int nwarps, int rows) {
+    using L = MergeLayout<D>;
+    float *cm = L::m(base, nwarps), *cl = L::l(base, nwarps), *co = L::o(base, nwarps);
+    for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+        const int r = idx / D, d = idx % D;
+        float M = -INFINITY;
+        for (int w = 0; w < nwarps; ++w) M = fmaxf(M, L::m(base, w)[r]);
+        float acc = 0.f;
+        if (M != -INFINITY)
+            for (int w = 0; w < nwarps; ++w)
+                acc += fast_exp2(L::m(base, w)[r] - M) * L::o(base, w)[r * L::kStride + d];
+        co[r * L::kStride + d] = acc;
+    }
+    if (threadIdx.x < rows) {
+        const int r = threadIdx.x;
+        float M = -INFINITY;
+        for (int w = 0; w < nwarps; ++w) M = fmaxf(M, L::m(base, w)[r]);
+        float s = 0.f;
+        if (M != -INFINITY)
+            for (int w = 0; w < nwarps; ++w) s += fast_exp2(L::m(base, w)[r] - M) * L::l(base, w)[r];
+        cm[r] = M;
+        cl[r] = s;
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void store_out(const DecodeParams &p, int64_t idx, float v) {
+    if (p.out_bf16)
+        reinterpret_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<float *>(p.out)[idx] = v;
+}
+
+// Write rows [0, rows) of the CTA result for (b, kv head g, head tile, partition).
+template <int D>
+__device__ void write_result(const DecodeParams &p, float *base, int nwarps, int b, int g,
+                             int tile, int part, int rows, int nparts) {
+    using L = MergeLayout<D>;
+    float *cm = L::m(base, nwarps), *cl = L::l(base, nwarps), *co = L::o(base, nwarps);
+    const int h0 = g * p.group + tile * kRowsPerTile;
+    const int mode = (p.mode == kModeFused && nparts <= 1) ? kModeFinal : p.mode;
+
+    if (mode == kModeFinal) {
+        for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+            const int r = idx / D, d = idx % D;
+            const float l = cl[r];
+            const float v = l > 0.f ? co[r * L::kStride + d] / l : 0.f;
+            store_out(p, (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + d, v);
+        }
+        return;
+    }
+    if (mode == kModeSplitK) {
+        const int P = p.nsplit;
+        for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+            const int r = idx / D, d = idx % D;
+            const float l = cl[r];
+            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * P + part;
+            p.tmp_out[row * D + d] = l > 0.f ? co[r * L::kStride + d] / l : 0.f;
+        }
+        if (threadIdx.x < rows) {
+            const int r = threadIdx.x;
+            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * P + part;
+            const float l = cl[r];
+            p.max_logits[row] = l > 0.f ? cm[r] * kLn2 : -INFINITY;
+            p.exp_sums[row] = l;
+        }
+        return;
+    }
+
+    // fused: publish this partition, the last CTA to arrive merges them all
+    const int S = p.nsplit;
+    for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+        const int r = idx / D, d = idx % D;
+        const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S + part;
+        p.ws_o[row * D + d] = co[r * L::kStride + d];
+    }
+    if (threadIdx.x < rows) {
+        const int r = threadIdx.x;
+        const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S + part;
+        p.ws_ml[row * 2 + 0] = cm[r];
+        p.ws_ml[row * 2 + 1] = cl[r];
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ unsigned s_last;
+    unsigned *counter = p.ws_count + (static_cast<int64_t>(b) * p.num_kv_heads + g) * p.ntile + tile;
+    if (threadIdx.x == 0) {
+        const unsigned prev = atomicAdd(counter, 1u);
+        s_last = (prev == static_cast<unsigned>(nparts - 1)) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    float *wgt = base + (nwarps + 1) * L::kRegion;  // [16][kMaxSplits]
+    __shared__ float s_inv[kRowsPerTile];
+    if (threadIdx.x < rows) {
+        const int r = threadIdx.x;
+        const int64_t row0 = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S;
+        float M = -INFINITY;
+        for (int q = 0; q < nparts; ++q) {
+            const float l = __ldcg(p.ws_ml + (row0 + q) * 2 + 1);
+            if (l > 0.f) M = fmaxf(M, __ldcg(p.ws_ml + (row0 + q) * 2 + 0));
+        }
+        float tot = 0.f;
+        for (int q = 0; q < nparts; ++q) {
+            const float l = __ldcg(p.ws_ml + (row0 + q) * 2 + 1);
+            const float w = l > 0.f ? fast_exp2(__ldcg(p.ws_ml + (row0 + q) * 2 + 0) - M) : 0.f;
+            wgt[r * kMaxSplits + q] = w;
+            tot += w * l;
+        }
+        s_inv[r] = tot > 0.f ? 1.f / tot : 0.f;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+        const int r = idx / D, d = idx % D;
+        const int64_t row0 = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S;
+        float acc = 0.f;
+        for (int q = 0; q < nparts; ++q) {
+            const float w = wgt[r * kMaxSplits + q];
+            if (w != 0.f) acc += w * __ldcg(p.ws_o + (row0 + q) * D + d);
+        }
+        store_out(p, (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + d, acc * s_inv[r]);
+    }
+    if (threadIdx.x == 0) *counter = 0u;  // ready for the next call
+}
+
+// A CTA whose partition holds no tokens.
+template <int D>
+__device__ void write_empty(const DecodeParams &p, int b, int g, int tile, int part, int rows,
+                            int nparts) {
+    const int h0 = g * p.group + tile * kRowsPerTile;
+    if (p.mode == kModeSplitK) {
+        const int P = p.nsplit;
+        for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+            const int r = idx / D, d = idx % D;
+            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * P + part;
+            p.tmp_out[row * D + d] = 0.f;
+        }
+        if (threadIdx.x < rows) {
+            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + threadIdx.x) * P + part;
+            p.max_logits[row] = -INFINITY;
+            p.exp_sums[row] = 0.f;
+        }
+        return;
+    }
+    // final / fused: an empty sequence has one all-zero output row, written by partition 0
+    if (nparts == 0 && part == 0)
+        for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+            const int r = idx / D, d = idx % D;
+            store_out(p, (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + d, 0.f);
+        }
+}
+
+}  // namespace pa

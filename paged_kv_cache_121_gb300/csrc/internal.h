@@ -1,0 +1,27 @@
+// Launchers shared between the translation units of libpa (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct DecodeParams;
+
+bool decode_mma_supported(int head_dim, int block_size);
+cudaError_t launch_decode_mma(const DecodeParams &p, const CUtensorMap &tmap_k,
+                              const CUtensorMap &tmap_v, dim3 grid, cudaStream_t stream);
+cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, cudaStream_t stream);
+cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
+                             const float *exp_sums, const int32_t *context_lens, int num_seqs,
+                             int num_heads, int head_dim, int max_partitions, int partition_size,
+                             cudaStream_t stream);
+cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
+                                     void *v_cache, const int64_t *slot_mapping, int num_tokens,
+                                     int64_t num_slots, int row_bytes, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
+                               int num_pairs, int64_t num_blocks, int64_t block_bytes,
+                               cudaStream_t stream);
+
+}  // namespace pa

@@ -296,12 +296,19 @@ def run_ours(args, rank, world, local_rank):
         scatter(v)
         decode(v)
 
-    # correctness of the timed configuration against the oracle (one sequence sample)
     for i in range(copies):
         step(i)
     torch.cuda.synchronize()
     if pa.pa_device_status() != 0:
         raise SystemExit("device status not clean after warm-up")
+    if args.profile_steps:
+        # a few eager steps and nothing else: the command ncu captures
+        for i in range(args.profile_steps):
+            step(i)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_steps": args.profile_steps, "config": desc,
+                          "workspace_bytes": int(ws_bytes)}), flush=True)
+        return 0
 
     # CUDA graphs: one graph per batch view, each holding one whole step
     stream = torch.cuda.Stream()
@@ -471,6 +478,8 @@ def main():
     ap.add_argument("--config", choices=["qwen3", "long", "gqa"], default="qwen3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many eager steps after the warm-up and exit (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

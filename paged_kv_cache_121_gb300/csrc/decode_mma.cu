@@ -330,7 +330,8 @@ static cudaError_t launch_impl(const DecodeParams &p, const CUtensorMap &tk, con
                                dim3 grid, cudaStream_t stream) {
     using C = MmaCfg<D, BS>;
     auto kern = decode_mma_kernel<D, BS>;
-    cudaError_t e = ensure_smem_limit(kern, C::kSmemBytes);
+    static unsigned long long done = 0;
+    cudaError_t e = ensure_smem_limit(kern, C::kSmemBytes, done);
     if (e != cudaSuccess) return e;
     kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p);
     return cudaGetLastError();

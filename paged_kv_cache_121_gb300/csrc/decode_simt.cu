@@ -147,7 +147,8 @@ template <int D, int MAXR, typename KV>
 static cudaError_t launch_simt_impl(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
     auto kern = decode_simt_kernel<D, MAXR, KV>;
     const size_t smem = MergeLayout<D>::bytes(4);
-    cudaError_t e = ensure_smem_limit(kern, smem);
+    static unsigned long long done = 0;
+    cudaError_t e = ensure_smem_limit(kern, smem, done);
     if (e != cudaSuccess) return e;
     kern<<<grid, 128, smem, stream>>>(p);
     return cudaGetLastError();
@@ -227,7 +228,8 @@ cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, cons
                              cudaStream_t stream) {
     const size_t smem = sizeof(float) * static_cast<size_t>(max_partitions);
     if (smem > 48 * 1024) {
-        cudaError_t e = ensure_smem_limit(lse_merge_kernel, 200 * 1024);
+        static unsigned long long done = 0;
+        cudaError_t e = ensure_smem_limit(lse_merge_kernel, 200 * 1024, done);
         if (e != cudaSuccess) return e;
     }
     dim3 grid(num_heads, num_seqs);

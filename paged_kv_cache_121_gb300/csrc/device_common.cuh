@@ -48,17 +48,17 @@ struct DecodeParams {
 };
 
 // Raise a kernel's dynamic shared-memory limit once per device (host side;
-// keeps the call out of CUDA-graph capture after the first launch).
+// keeps the call out of CUDA-graph capture after the first launch). Each
+// kernel instantiation passes its own `done` mask (bit d: device d set up).
 template <typename Kernel>
-inline cudaError_t ensure_smem_limit(Kernel kern, size_t bytes) {
-    static unsigned long long done_mask = 0;  // bit d: device d configured
+inline cudaError_t ensure_smem_limit(Kernel kern, size_t bytes, unsigned long long &done) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
-    if (bit && (__atomic_load_n(&done_mask, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+    if (bit && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-    if (e == cudaSuccess && bit) __atomic_fetch_or(&done_mask, bit, __ATOMIC_ACQ_REL);
+    if (e == cudaSuccess && bit) __atomic_fetch_or(&done, bit, __ATOMIC_ACQ_REL);
     return e;
 }
 

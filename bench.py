@@ -49,7 +49,7 @@ def build_workload(config: str, rank: int, copies: int):
     if config == "qwen3":
         return workloads.qwen3(num_seqs=16, copies=copies), "qwen3-8b layer: 16 seqs x 4164 tokens, Hq 32, Hkv 8, D 128, bf16, block 16, pool 38348 blocks"
     if config == "long":
-        return workloads.long_context(block_size=16, num_seqs=4 * copies), "long context: 4 seqs x 32768 tokens, Hq 64, Hkv 8, D 128, bf16, block 16"
+        return workloads.long_context(block_size=16, num_seqs=4, copies=copies), "long context: 4 seqs x 32768 tokens, Hq 64, Hkv 8, D 128, bf16, block 16"
     if config == "gqa":
         return workloads.gqa(num_seqs=64 * copies, num_blocks=20000 * copies), "llama gqa: 64 seqs, len U[512,4096], Hq 32, Hkv 8, D 128, bf16, block 16"
     raise SystemExit(f"unknown config {config}")
@@ -453,7 +453,7 @@ def run_ours(args, rank, world, local_rank):
         "pct_of_measured_hbm": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "decode_mma_kernel<128,%d>" % bs, "peak_kind": peak_kind,
+                     "kernel": "decode_mma_kernel<128,%d>" % min(bs, 16), "peak_kind": peak_kind,
                      "decode_us": decode_ms * 1e3, "alg_bytes_per_launch": int(alg)},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),

@@ -24,7 +24,10 @@ __device__ int g_device_status;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kCtasPerSm = 2;         // resident decode CTAs per SM the split plan aims at
+constexpr int kCtasPerSmMma = 2;      // resident CTAs per SM the split plan aims at
+constexpr int kCtasPerSmSimt = 2;     //   (tensor-core / CUDA-core kernel)
+constexpr int kMmaHeadsPerCta = 4;    // KV heads per tensor-core CTA (consumer warps)
+constexpr int kMmaRingKiB = 96;       // shared-memory ring per tensor-core CTA
 constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
 
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -66,14 +69,27 @@ int *status_word(int dev) {
     return static_cast<int *>(addr);
 }
 
-// Optional tuning knob read once: resident CTAs per SM assumed by the split plan.
-int ctas_per_sm_target() {
-    static const int v = [] {
-        const char *e = std::getenv("PA_DECODE_CTAS_PER_SM");
-        const int x = e ? std::atoi(e) : 0;
-        return (x >= 1 && x <= 64) ? x : kCtasPerSm;
-    }();
+int env_int(const char *name, int lo, int hi) {
+    const char *e = std::getenv(name);
+    const int x = e ? std::atoi(e) : 0;
+    return (x >= lo && x <= hi) ? x : 0;
+}
+
+// Optional tuning knobs, read once (0 = the built-in default):
+//   PA_DECODE_CTAS_PER_SM  CTAs per SM the split plan aims at
+//   PA_DECODE_HEADS        KV heads per tensor-core CTA (1..8)
+//   PA_DECODE_RING_KB      shared-memory ring per tensor-core CTA (KiB)
+int ctas_per_sm_override() {
+    static const int v = env_int("PA_DECODE_CTAS_PER_SM", 1, 64);
     return v;
+}
+int heads_cap() {
+    static const int v = env_int("PA_DECODE_HEADS", 1, 8);
+    return v ? v : kMmaHeadsPerCta;
+}
+int ring_kb() {
+    static const int v = env_int("PA_DECODE_RING_KB", 16, 200);
+    return v ? v : kMmaRingKiB;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -90,17 +106,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 4-D view of a bf16 cache [num_blocks, block_size, Hkv, D] (innermost first:
-// D, Hkv, block_size, num_blocks); box = 64 dims x 1 head x block_size tokens
+// D, Hkv, block_size, num_blocks); box = 64 dims x 1 head x box_tokens tokens
 // x 1 block, 128-byte swizzle. Out-of-range block ids read as zeros.
 pa_status make_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int block_size,
-                         int num_kv_heads, int head_dim) {
+                         int num_kv_heads, int head_dim, int box_tokens) {
     auto enc = tensor_map_encoder();
     if (!enc) return PA_ERR_CUDA;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
                                 static_cast<cuuint64_t>(block_size), static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
     const cuuint64_t strides[3] = {row, row * num_kv_heads, row * num_kv_heads * block_size};
-    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(block_size), 1};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_tokens), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -128,20 +144,29 @@ pa_status check_shape(const DecodeShape &s) {
 }
 
 struct Plan {
+    bool mma;
+    bool cluster;       // split merged through distributed shared memory (no workspace)
+    int heads_per_cta;
     int ntile;
     int nsplit;
     int part_blocks;
 };
 
-// Split each (sequence, KV head, head tile) context so that about
+bool use_mma(const DecodeShape &s, bool bf16) { return bf16 && decode_mma_supported(s.head_dim, s.block_size); }
+
+// Split each (sequence, KV-head group, head tile) context so that about
 // sm_count * ctas_per_sm CTAs exist, with at least kMinSplitTokens per piece.
-Plan plan_split(const DecodeShape &s, int sms) {
+Plan plan_split(const DecodeShape &s, int sms, bool mma) {
     Plan pl;
+    pl.mma = mma;
+    pl.heads_per_cta = mma ? decode_mma_heads_per_cta(s.num_kv_heads, heads_cap()) : 1;
     const int group = s.num_heads / s.num_kv_heads;
     pl.ntile = (group + kRowsPerTile - 1) / kRowsPerTile;
-    const int64_t units = static_cast<int64_t>(s.num_seqs) * s.num_kv_heads * pl.ntile;
+    const int64_t units =
+        static_cast<int64_t>(s.num_seqs) * (s.num_kv_heads / pl.heads_per_cta) * pl.ntile;
     const int64_t nblk = std::max<int64_t>(1, cdiv64(s.max_ctx, s.block_size));
-    const int64_t cap = static_cast<int64_t>(sms) * ctas_per_sm_target();
+    const int per_sm = ctas_per_sm_override() ? ctas_per_sm_override() : (mma ? kCtasPerSmMma : kCtasPerSmSimt);
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
     int64_t nsplit = 1;
     if (units > 0 && units < cap) {
         nsplit = cap / units;
@@ -149,9 +174,22 @@ Plan plan_split(const DecodeShape &s, int sms) {
         nsplit = std::min(nsplit, std::max<int64_t>(1, nblk / min_pb));
         nsplit = std::min<int64_t>(nsplit, kMaxSplits);
     }
+    // Tensor-core kernel: merge inside a cluster when the split fits one
+    // (or when trimming it to one still leaves ~3/4 of the CTA slots busy).
+    pl.cluster = false;
+    if (mma && nsplit >= 2) {
+        if (nsplit > kMaxClusterSplits && units * kMaxClusterSplits * 4 >= cap * 3)
+            nsplit = kMaxClusterSplits;
+        pl.cluster = nsplit <= kMaxClusterSplits;
+    }
     const int64_t pb = cdiv64(nblk, nsplit);
     pl.part_blocks = static_cast<int>(pb);
     pl.nsplit = static_cast<int>(cdiv64(nblk, pb));
+    if (pl.nsplit < 2) pl.cluster = false;
+    if (pl.cluster) {
+        // the cluster must span exactly the partitions of one context
+        pl.nsplit = static_cast<int>(nsplit);
+    }
     return pl;
 }
 
@@ -161,7 +199,7 @@ struct WorkspaceLayout {
 
 WorkspaceLayout workspace_layout(const DecodeShape &s, const Plan &pl) {
     WorkspaceLayout w{};
-    if (pl.nsplit <= 1) return w;
+    if (pl.nsplit <= 1 || pl.cluster) return w;
     const size_t rows = static_cast<size_t>(s.num_seqs) * s.num_heads * pl.nsplit;
     w.o_off = 0;
     w.ml_off = align256(rows * s.head_dim * sizeof(float));
@@ -184,13 +222,21 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
     p.status = status_word(dev);
     if (!p.status) return PA_ERR_CUDA;
     const dim3 grid(static_cast<unsigned>(p.nsplit),
-                    static_cast<unsigned>(s.num_kv_heads * p.ntile), static_cast<unsigned>(s.num_seqs));
+                    static_cast<unsigned>((s.num_kv_heads / p.heads_per_cta) * p.ntile),
+                    static_cast<unsigned>(s.num_seqs));
     cudaError_t e;
-    if (bf16 && decode_mma_supported(s.head_dim, s.block_size)) {
+    if (use_mma(s, bf16)) {
+        const int tt = decode_mma_tile_tokens(s.block_size);
+        const int stage = decode_mma_stage_bytes(s.head_dim, s.block_size, p.heads_per_cta);
+        p.ring_bytes = std::max(stage, (ring_kb() * 1024) / stage * stage);
+        if (p.cluster_merge) {
+            const int need = decode_mma_cluster_bytes(s.head_dim, p.heads_per_cta);
+            if (p.ring_bytes < need) p.ring_bytes = static_cast<int>(cdiv64(need, stage) * stage);
+        }
         CUtensorMap tk, tv;
-        pa_status st = make_cache_map(&tk, p.k_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim);
+        pa_status st = make_cache_map(&tk, p.k_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim, tt);
         if (st != PA_OK) return st;
-        st = make_cache_map(&tv, p.v_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim);
+        st = make_cache_map(&tv, p.v_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim, tt);
         if (st != PA_OK) return st;
         e = launch_decode_mma(p, tk, tv, grid, stream);
     } else {
@@ -290,7 +336,8 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_h
     if (current_device(&dev) != PA_OK) return 0;
     const int sms = sm_count(dev);
     if (sms <= 0) return 0;
-    return workspace_layout(s, plan_split(s, sms)).total;
+    return std::max(workspace_layout(s, plan_split(s, sms, true)).total,
+                    workspace_layout(s, plan_split(s, sms, false)).total);
 }
 
 PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
@@ -315,20 +362,33 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
     const int sms = sm_count(dev);
     if (sms <= 0) return PA_ERR_CUDA;
 
-    Plan pl = plan_split(s, sms);
+    Plan pl = plan_split(s, sms, use_mma(s, kv_dtype == PA_BF16));
     DecodeParams p;
     fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
     p.out = out;
     p.out_bf16 = out_dtype == PA_BF16;
     p.ntile = pl.ntile;
-    if (workspace == nullptr && workspace_bytes == 0) {
-        // no scratch: one CTA per (sequence, KV head, head tile)
-        pl.part_blocks = std::max(1, (max_context_len + block_size - 1) / block_size);
-        pl.nsplit = 1;
+    p.heads_per_cta = pl.heads_per_cta;
+    if (workspace == nullptr && workspace_bytes == 0 && !pl.cluster) {
+        // no scratch: the tensor-core kernel keeps a split it can merge within
+        // a cluster; otherwise one CTA per (sequence, KV-head group, head tile)
+        const int64_t nblk = std::max<int64_t>(1, cdiv64(max_context_len, block_size));
+        if (pl.mma && pl.nsplit > 1) {
+            const int64_t pb = cdiv64(nblk, std::min(pl.nsplit, kMaxClusterSplits));
+            pl.part_blocks = static_cast<int>(pb);
+            pl.nsplit = static_cast<int>(cdiv64(nblk, pb));
+            pl.cluster = pl.nsplit > 1;
+        } else {
+            pl.part_blocks = static_cast<int>(nblk);
+            pl.nsplit = 1;
+        }
     }
     p.nsplit = pl.nsplit;
     p.part_blocks = pl.part_blocks;
-    if (pl.nsplit > 1) {
+    p.cluster_merge = pl.cluster ? 1 : 0;
+    if (pl.cluster) {
+        p.mode = kModeFused;
+    } else if (pl.nsplit > 1) {
         const WorkspaceLayout wl = workspace_layout(s, pl);
         if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
         char *ws = static_cast<char *>(workspace);
@@ -371,6 +431,7 @@ PA_API pa_status pa_decode_splitk(float *tmp_out, float *max_logits, float *exp_
     p.max_logits = max_logits;
     p.exp_sums = exp_sums;
     p.ntile = (s.num_heads / s.num_kv_heads + kRowsPerTile - 1) / kRowsPerTile;
+    p.heads_per_cta = use_mma(s, kv_dtype == PA_BF16) ? decode_mma_heads_per_cta(s.num_kv_heads, heads_cap()) : 1;
     p.nsplit = static_cast<int>(P);
     p.part_blocks = partition_size / block_size;
     p.mode = kModeSplitK;

@@ -6,51 +6,55 @@
 // sections 8 and 14; "PagedAttention, explained.", procedure step 5). Query
 // head h reads KV head h / (Hq / Hkv).
 //
-// How (one CTA = one sequence x one KV head x up to 16 of its query heads x
-// one partition of its blocks):
-//  * warp 4 (one elected lane) walks the block table and issues TMA tiled
-//    loads (cp.async.bulk.tensor) of each physical block's K and V rows for
-//    this KV head into a ring of shared-memory stages, completion counted on
-//    mbarriers. The tile is the page: block_size rows of head_dim bf16,
-//    loaded as 64-dim halves with the 128-byte swizzle so that the matrix
-//    loads below are bank-conflict free.
-//  * warps 0-3 take the stages round-robin. S = Q K^T runs on the tensor
-//    cores with mma.m16n8k16 (M = query heads of the GQA group, N = tokens,
-//    K = head dims), Q living in registers for the whole CTA. Online softmax
-//    in base 2 (scores pre-multiplied by scale*log2 e) with the running max
-//    and sum per row; P is split into a bf16 high part and a bf16 residual
-//    so that P.V (mma with M = heads, N = head dims, K = tokens) keeps ~16
-//    bits of P. A consumer releases its stage with an mbarrier arrive.
-//  * tokens past the context in the last block are masked (score -inf, V
-//    rows zeroed in shared memory, so stale or NaN slot contents never leak).
-//  * the four warps' softmax states are merged in shared memory and handed to
-//    the shared epilogue (final output, split-K partition, or fused
-//    last-CTA log-sum-exp merge).
+// How. One CTA = one sequence x a group of up to 8 KV heads x up to 16 query
+// heads per KV head x one partition of the sequence's blocks.
+//  * The last warp walks the block table (read 32 entries at a time, a chunk
+//    ahead) and, per tile of 16 tokens (8 when blocks are 8 tokens), issues
+//    TMA tiled loads (cp.async.bulk.tensor) of the tile's K and V rows for
+//    every KV head of the group into one stage of a shared-memory ring;
+//    completion is counted on the stage's mbarrier. All heads of a block are
+//    requested back to back, so each block's K (and V) -- contiguous in the
+//    [num_blocks, block_size, Hkv, D] layout -- is fetched as one burst.
+//    Rows land as 64-dim halves with the 128-byte swizzle, which makes the
+//    matrix loads below bank-conflict free.
+//  * Consumer warp j owns KV head j of the group for the whole CTA and reads
+//    every stage. S = Q K^T runs on the tensor cores (mma.m16n8k16, M = the
+//    query heads of the GQA group, N = tokens, K = head dims; Q stays in
+//    registers). Online softmax in base 2 with a running max and sum per row.
+//    P is split into a bf16 high part and a bf16 residual so that P.V (M =
+//    heads, N = head dims, K = tokens) keeps ~16 bits of P. Each warp
+//    releases the stage with one mbarrier arrive; the stage is refilled once
+//    every head's warp has released it.
+//  * Tokens past the context in the last tile are masked (score -inf, V rows
+//    zeroed in shared memory, so stale or NaN slot contents never leak).
+//  * Each warp finishes its own head from registers: the final output, a
+//    split-K partition, or (fused split) its partition followed by an
+//    arrival count; the last partition to arrive merges them by log-sum-exp.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the device status word, drains its own copies and returns.
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "internal.h"
 
 namespace pa {
 
-template <int D, int BS>
+template <int D, int TT>
 struct MmaCfg {
-    static constexpr int kConsumerWarps = 4;
-    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+    static constexpr int kMaxHeads = 8;                 // KV heads per CTA = consumer warps
+    static constexpr int kThreads = 32 * (kMaxHeads + 1);
     static constexpr int kHalves = D / 64;
-    static constexpr int kHalfBytes = BS * 128;      // one 64-dim half of a K or V tile
-    static constexpr int kTileBytes = BS * D * 2;    // K (or V) rows of one block, one head
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kRawStages = (64 * 1024) / kStageBytes;
-    static constexpr int kStages = kRawStages > 16 ? 16 : kRawStages;
-    static constexpr size_t kMergeBytes = MergeLayout<D>::bytes(kConsumerWarps);
-    static constexpr size_t kRingBytes = static_cast<size_t>(kStages) * kStageBytes;
-    static constexpr size_t kDataBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
-    static constexpr size_t kSmemBytes = 1024 + kDataBytes + 2 * kStages * sizeof(uint64_t);
-    static_assert(kStages % kConsumerWarps == 0, "stage ring must be a multiple of the consumer warps");
+    static constexpr int kHalfBytes = TT * 128;         // one 64-dim half of one head's tile
+    static constexpr int kHeadBytes = TT * D * 2;       // one head's K (or V) rows of a tile
+    static constexpr int kMaxRingBytes = 200 * 1024;
+    static constexpr int kMaxStages = 32;
+    static constexpr size_t kBarrierBytes = 2 * kMaxStages * sizeof(uint64_t);
+    static size_t smem_bytes(int ring) { return 1024 + static_cast<size_t>(ring) + kBarrierBytes; }
     static_assert(kHalfBytes % 1024 == 0, "swizzled halves must stay 1024-byte aligned");
-    static_assert(BS % 8 == 0 && BS <= 32, "block size must be 8, 16 or 32");
+    static_assert(TT == 8 || TT == 16, "tiles are 8 or 16 tokens");
 };
+
+constexpr float kRescaleSlack = 8.f;   // base-2 headroom before the running max is moved
 
 __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &hi, uint32_t &lo) {
     hi = pack_bf16x2(x, y);
@@ -59,38 +63,288 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &hi, uin
     lo = pack_bf16x2(x - hx, y - hy);
 }
 
-template <int D, int BS>
-__global__ void __launch_bounds__(MmaCfg<D, BS>::kThreads, 2)
+__device__ __forceinline__ void store_out2(const DecodeParams &p, int64_t idx, float a, float c) {
+    if (p.out_bf16)
+        *reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(p.out) + idx) = pack_bf16x2(a, c);
+    else
+        *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + idx) = make_float2(a, c);
+}
+
+__device__ __forceinline__ float vec_get(const float4 &v, int e) {
+    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ float vec_get(const float2 &v, int e) { return e == 0 ? v.x : v.y; }
+
+// One warp's softmax state for 16 query rows of one KV head, in the mma
+// accumulator layout: lane (r = lane/4, q = lane%4) holds rows r and r+8,
+// dims 8*dn + 2q and +1 of every 8-dim slice dn.
+template <int D>
+struct WarpState {
+    float o[D / 8][4];
+    float m0, m1, l0, l1;   // reference max (base 2) and sum of 2^(s - m) per row
+    float t0, t1;           // true running max of the scores (base 2)
+};
+
+// Write a warp's result (final output, split-K partition, or fused partition
+// + last-arrival merge) for query heads h0 .. h0+rows-1.
+template <int D>
+__device__ __forceinline__ void warp_epilogue(const DecodeParams &p, WarpState<D> &st, int b, int gh, int tile,
+                              int part, int h0, int rows, int nparts, int lane) {
+    const int r = lane >> 2, q4 = lane & 3;
+    const int mode = (p.mode == kModeFused && nparts <= 1) ? kModeFinal : p.mode;
+    const bool v0 = r < rows, v1 = r + 8 < rows;
+    if (mode == kModeFinal) {
+        const float i0 = st.l0 > 0.f ? 1.f / st.l0 : 0.f, i1 = st.l1 > 0.f ? 1.f / st.l1 : 0.f;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+            const int d = 8 * dn + 2 * q4;
+            if (v0) store_out2(p, (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + d,
+                               st.o[dn][0] * i0, st.o[dn][1] * i0);
+            if (v1) store_out2(p, (static_cast<int64_t>(b) * p.num_heads + h0 + r + 8) * D + d,
+                               st.o[dn][2] * i1, st.o[dn][3] * i1);
+        }
+        return;
+    }
+    const int S = p.nsplit;
+    const int64_t row0 = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S + part;
+    const int64_t row1 = row0 + 8 * static_cast<int64_t>(S);
+    if (mode == kModeSplitK) {
+        const float i0 = st.l0 > 0.f ? 1.f / st.l0 : 0.f, i1 = st.l1 > 0.f ? 1.f / st.l1 : 0.f;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+            const int d = 8 * dn + 2 * q4;
+            if (v0) *reinterpret_cast<float2 *>(p.tmp_out + row0 * D + d) = make_float2(st.o[dn][0] * i0, st.o[dn][1] * i0);
+            if (v1) *reinterpret_cast<float2 *>(p.tmp_out + row1 * D + d) = make_float2(st.o[dn][2] * i1, st.o[dn][3] * i1);
+        }
+        if (q4 == 0) {   // report the true max: sum of 2^(s - t) = l * 2^(m - t)
+            if (v0) {
+                p.max_logits[row0] = st.l0 > 0.f ? st.t0 * kLn2 : -INFINITY;
+                p.exp_sums[row0] = st.l0 > 0.f ? st.l0 * fast_exp2(st.m0 - st.t0) : 0.f;
+            }
+            if (v1) {
+                p.max_logits[row1] = st.l1 > 0.f ? st.t1 * kLn2 : -INFINITY;
+                p.exp_sums[row1] = st.l1 > 0.f ? st.l1 * fast_exp2(st.m1 - st.t1) : 0.f;
+            }
+        }
+        return;
+    }
+    // fused: publish this partition (unnormalised), count arrivals, last one merges
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+        const int d = 8 * dn + 2 * q4;
+        if (v0) *reinterpret_cast<float2 *>(p.ws_o + row0 * D + d) = make_float2(st.o[dn][0], st.o[dn][1]);
+        if (v1) *reinterpret_cast<float2 *>(p.ws_o + row1 * D + d) = make_float2(st.o[dn][2], st.o[dn][3]);
+    }
+    if (q4 == 0) {
+        if (v0) *reinterpret_cast<float2 *>(p.ws_ml + row0 * 2) = make_float2(st.m0, st.l0);
+        if (v1) *reinterpret_cast<float2 *>(p.ws_ml + row1 * 2) = make_float2(st.m1, st.l1);
+    }
+    __threadfence();
+    __syncwarp();
+    unsigned *counter = p.ws_count + (static_cast<int64_t>(b) * p.num_kv_heads + gh) * p.ntile + tile;
+    unsigned last = 0;
+    if (lane == 0) last = atomicAdd(counter, 1u) == static_cast<unsigned>(nparts - 1) ? 1u : 0u;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    // Merge, two query rows at a time. Each lane owns D/32 consecutive dims and
+    // reads them as one vector per (row, partition); lane j also reads the
+    // (max, sum) of partition j (and j + 32). All those loads are issued
+    // before any of them is used, so the whole merge costs about one L2 round
+    // trip per chunk of kMergeChunk partitions instead of one per partition.
+    constexpr int kVec = D / 32;
+    using VecT = typename std::conditional<kVec == 4, float4, float2>::type;
+    constexpr int kMergeChunk = 12;
+    for (int rg = 0; rg < rows; rg += 2) {
+        const bool live1 = rg + 1 < rows;
+        const int64_t base0 = (static_cast<int64_t>(b) * p.num_heads + h0 + rg) * S;
+        const int64_t base1 = base0 + S;
+        float2 mla[2], mlb[2];
+        mla[0] = mla[1] = mlb[0] = mlb[1] = make_float2(-INFINITY, 0.f);
+        if (lane < nparts) {
+            mla[0] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + (base0 + lane) * 2));
+            if (live1) mla[1] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + (base1 + lane) * 2));
+        }
+        if (lane + 32 < nparts) {
+            mlb[0] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + (base0 + lane + 32) * 2));
+            if (live1) mlb[1] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + (base1 + lane + 32) * 2));
+        }
+        const VecT *src0 = reinterpret_cast<const VecT *>(p.ws_o + base0 * D) + lane;
+        const VecT *src1 = reinterpret_cast<const VecT *>(p.ws_o + base1 * D) + lane;
+        constexpr int kStride = D / kVec;   // VecT elements per partition row
+        VecT v0[kMergeChunk], v1[kMergeChunk];
+#pragma unroll
+        for (int qq = 0; qq < kMergeChunk; ++qq) {
+            if (qq < nparts) v0[qq] = __ldcg(src0 + qq * kStride);
+            if (qq < nparts && live1) v1[qq] = __ldcg(src1 + qq * kStride);
+        }
+        float wa[2], wb[2], inv[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float M = fmaxf(mla[j].y > 0.f ? mla[j].x : -INFINITY, mlb[j].y > 0.f ? mlb[j].x : -INFINITY);
+#pragma unroll
+            for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            wa[j] = (mla[j].y > 0.f && M != -INFINITY) ? fast_exp2(mla[j].x - M) : 0.f;
+            wb[j] = (mlb[j].y > 0.f && M != -INFINITY) ? fast_exp2(mlb[j].x - M) : 0.f;
+            float L = wa[j] * mla[j].y + wb[j] * mlb[j].y;
+#pragma unroll
+            for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+            inv[j] = L > 0.f ? 1.f / L : 0.f;
+        }
+        float acc0[kVec], acc1[kVec];
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) acc0[e] = acc1[e] = 0.f;
+        for (int q0 = 0; q0 < nparts; q0 += kMergeChunk) {
+            if (q0 > 0) {   // later chunks (more than kMergeChunk partitions)
+#pragma unroll
+                for (int qq = 0; qq < kMergeChunk; ++qq) {
+                    if (q0 + qq < nparts) v0[qq] = __ldcg(src0 + (q0 + qq) * kStride);
+                    if (q0 + qq < nparts && live1) v1[qq] = __ldcg(src1 + (q0 + qq) * kStride);
+                }
+            }
+#pragma unroll
+            for (int qq = 0; qq < kMergeChunk; ++qq) {
+                const int q = q0 + qq;
+                if (q < nparts) {   // warp-uniform
+                    const float w0 = __shfl_sync(0xffffffffu, q < 32 ? wa[0] : wb[0], q & 31);
+                    const float w1 = __shfl_sync(0xffffffffu, q < 32 ? wa[1] : wb[1], q & 31);
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) acc0[e] += w0 * vec_get(v0[qq], e);
+                    if (live1) {
+#pragma unroll
+                        for (int e = 0; e < kVec; ++e) acc1[e] += w1 * vec_get(v1[qq], e);
+                    }
+                }
+            }
+        }
+        const int64_t o0 = (static_cast<int64_t>(b) * p.num_heads + h0 + rg) * D + lane * kVec;
+#pragma unroll
+        for (int e = 0; e < kVec; e += 2) {
+            store_out2(p, o0 + e, acc0[e] * inv[0], acc0[e + 1] * inv[0]);
+            if (live1) store_out2(p, o0 + D + e, acc1[e] * inv[1], acc1[e + 1] * inv[1]);
+        }
+    }
+    if (lane == 0) *counter = 0u;   // ready for the next call
+}
+
+// Split merged inside a thread-block cluster: the cluster is the nsplit
+// partitions of one (sequence, KV-head group, head tile). Each CTA leaves the
+// per-head softmax states of its partition in its own shared memory (m[16],
+// l[16], O[16][D] per head); after a cluster barrier every CTA merges a slice
+// of the outputs by reading all partitions straight from its peers' shared
+// memory; a second barrier keeps each CTA (and its shared memory) alive until
+// every peer is done reading it. No global workspace, no atomics.
+template <int D>
+__device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, const WarpState<D> &st, float *sm, int b,
+                                       int hgrp, int tile, int rows, int warp, int lane) {
+    constexpr int kRegion = 32 + kRowsPerTile * D;   // floats per head
+    const int hpc = p.heads_per_cta;
+    if (warp < hpc) {
+        float *reg = sm + warp * kRegion;
+        const int r = lane >> 2, q4 = lane & 3;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+            const int d = 8 * dn + 2 * q4;
+            *reinterpret_cast<float2 *>(reg + 32 + r * D + d) = make_float2(st.o[dn][0], st.o[dn][1]);
+            *reinterpret_cast<float2 *>(reg + 32 + (r + 8) * D + d) = make_float2(st.o[dn][2], st.o[dn][3]);
+        }
+        if (q4 == 0) {
+            reg[r] = st.m0;
+            reg[r + 8] = st.m1;
+            reg[16 + r] = st.l0;
+            reg[16 + r + 8] = st.l1;
+        }
+    }
+    cluster_sync_all();   // every partition's state is now readable cluster-wide
+
+    const int ns = p.nsplit;                 // cluster size
+    const int rank = static_cast<int>(cluster_rank());
+    const int total = hpc * rows * D;
+    const int chunk = (total + ns - 1) / ns;
+    const int begin = rank * chunk;
+    const int end = min(total, begin + chunk);
+    const uint32_t base = smem_addr(sm);
+    for (int idx = begin + static_cast<int>(threadIdx.x); idx < end; idx += blockDim.x) {
+        const int j = idx / (rows * D);
+        const int rem = idx - j * rows * D;
+        const int rr = rem / D, d = rem - rr * D;
+        const uint32_t ml_off = base + 4u * static_cast<uint32_t>(j * kRegion + rr);
+        const uint32_t o_off = base + 4u * static_cast<uint32_t>(j * kRegion + 32 + rr * D + d);
+        float mq[8], lq[8], oq[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (q < ns) {
+                mq[q] = ld_cluster_f32(cluster_map(ml_off, q));
+                lq[q] = ld_cluster_f32(cluster_map(ml_off + 64u, q));
+                oq[q] = ld_cluster_f32(cluster_map(o_off, q));
+            } else {
+                mq[q] = -INFINITY;
+                lq[q] = 0.f;
+                oq[q] = 0.f;
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (lq[q] > 0.f) M = fmaxf(M, mq[q]);
+        float L = 0.f, acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (lq[q] > 0.f) {
+                const float wq = fast_exp2(mq[q] - M);
+                L += wq * lq[q];
+                acc += wq * oq[q];
+            }
+        const int h = (hgrp * hpc + j) * p.group + tile * kRowsPerTile + rr;
+        store_out(p, (static_cast<int64_t>(b) * p.num_heads + h) * D + d, L > 0.f ? acc / L : 0.f);
+    }
+    cluster_sync_all();   // peers have finished reading this CTA's shared memory
+}
+
+template <int D, int TT>
+__global__ void __launch_bounds__(MmaCfg<D, TT>::kThreads, 1)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ DecodeParams p) {
-    using C = MmaCfg<D, BS>;
-    constexpr int kStages = C::kStages;
-    constexpr int kNT = BS / 8;  // n-tiles of 8 tokens per block
+    using C = MmaCfg<D, TT>;
+    constexpr int kNT = TT / 8;  // n-tiles of 8 tokens per tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kDataBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.ring_bytes);
     __shared__ int s_abort;
     __shared__ int s_issued;
 
+    const int hpc = p.heads_per_cta;
     const int part = blockIdx.x;
-    const int g = blockIdx.y / p.ntile;
+    const int hgrp = blockIdx.y / p.ntile;
     const int tile = blockIdx.y % p.ntile;
     const int b = blockIdx.z;
     const int rows = min(kRowsPerTile, p.group - tile * kRowsPerTile);
     const SeqWork w = seq_work(p, b, part);
-    if (w.blk_begin >= w.blk_end) {
-        write_empty<D>(p, b, g, tile, part, rows, w.nparts);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool cluster = p.cluster_merge != 0;
+    if (w.blk_begin >= w.blk_end && !cluster) {
+        if (warp < hpc) {
+            const int gh = hgrp * hpc + warp;
+            warp_write_empty<D>(p, b, gh * p.group + tile * kRowsPerTile, part, rows, w.nparts, lane);
+        }
         return;
     }
-    const int ntiles = w.blk_end - w.blk_begin;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // (in a cluster every CTA takes part in the exchange, an empty partition included)
+    const int tok_begin = w.blk_begin * p.block_size;
+    const int tok_end = min(w.len, w.blk_end * p.block_size);
+    const int ntiles = tok_end > tok_begin ? (tok_end - tok_begin + TT - 1) / TT : 0;
+    const int tiles_per_block = p.block_size / TT;
+    const int stage_bytes = 2 * hpc * C::kHeadBytes;
+    int nstages = p.ring_bytes / stage_bytes;
+    if (nstages > C::kMaxStages) nstages = C::kMaxStages;
+    const int v_off = hpc * C::kHeadBytes;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < nstages; ++s) {
             mbar_init(smem_addr(&bars[s]), 1);
-            mbar_init(smem_addr(&bars[kStages + s]), 1);
+            mbar_init(smem_addr(&bars[C::kMaxStages + s]), hpc);
         }
         s_abort = 0;
         s_issued = 0;
@@ -98,50 +352,70 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     __syncthreads();
 
-    float o[D / 8][4];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    WarpState<D> st;
+    st.m0 = st.m1 = st.t0 = st.t1 = -INFINITY;
+    st.l0 = st.l1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < D / 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
 
-    if (warp == C::kConsumerWarps) {
+    if (warp == hpc) {
         // ------------------------------ producer ------------------------------
+        const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks + w.blk_begin;
+        uint64_t policy = 0;
         if (lane == 0) {
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
-            const uint64_t policy = l2_policy_evict_first();
-            const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
-            int issued = 0;
-            for (int i = 0; i < ntiles; ++i) {
-                const int s = i % kStages, k = i / kStages;
+            policy = l2_policy_evict_first();
+        }
+        // entry for tile i = table[i / tiles_per_block], fetched 32 tiles at a time, one chunk ahead
+        int cur = lane < ntiles ? table[lane / tiles_per_block] : 0;
+        int nxt = 32 + lane < ntiles ? table[(32 + lane) / tiles_per_block] : 0;
+        int issued = 0;
+        const int head0 = hgrp * hpc;
+        for (int i = 0; i < ntiles; ++i) {
+            if ((i & 31) == 0 && i > 0) {
+                cur = nxt;
+                nxt = i + 32 + lane < ntiles ? table[(i + 32 + lane) / tiles_per_block] : 0;
+            }
+            const int phys = __shfl_sync(0xffffffffu, cur, i & 31);
+            int ok = 1;
+            if (lane == 0) {
+                const int s = i % nstages, k = i / nstages;
                 if (k > 0) {
-                    if (*reinterpret_cast<volatile int *>(&s_abort)) break;
-                    if (!mbar_wait(smem_addr(&bars[kStages + s]), (k - 1) & 1)) {
+                    if (*reinterpret_cast<volatile int *>(&s_abort)) {
+                        ok = 0;
+                    } else if (!mbar_wait(smem_addr(&bars[C::kMaxStages + s]), (k - 1) & 1)) {
                         record_status(p.status, kStatusTimeout);
                         s_abort = 1;
-                        break;
+                        ok = 0;
                     }
                 }
-                const int phys = table[w.blk_begin + i];
-                const uint32_t full = smem_addr(&bars[s]);
-                mbar_arrive_expect_tx(full, C::kStageBytes);
-                const uint32_t kdst = smem_addr(smem + s * C::kStageBytes);
-                const uint32_t vdst = kdst + C::kTileBytes;
+                if (ok) {
+                    const uint32_t full = smem_addr(&bars[s]);
+                    mbar_arrive_expect_tx(full, static_cast<uint32_t>(stage_bytes));
+                    const uint32_t kdst = smem_addr(smem + s * stage_bytes);
+                    const int tok0 = (i % tiles_per_block) * TT;
+                    for (int h = 0; h < hpc; ++h) {
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h) {
-                    tma_load_4d(kdst + h * C::kHalfBytes, &tmap_k, h * 64, g, 0, phys, full, policy);
-                    tma_load_4d(vdst + h * C::kHalfBytes, &tmap_v, h * 64, g, 0, phys, full, policy);
+                        for (int hh = 0; hh < C::kHalves; ++hh) {
+                            const uint32_t off = h * C::kHeadBytes + hh * C::kHalfBytes;
+                            tma_load_4d(kdst + off, &tmap_k, hh * 64, head0 + h, tok0, phys, full, policy);
+                            tma_load_4d(kdst + v_off + off, &tmap_v, hh * 64, head0 + h, tok0, phys, full, policy);
+                        }
+                    }
+                    issued = i + 1;
                 }
-                issued = i + 1;
             }
-            s_issued = issued;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
-    } else {
+        if (lane == 0) s_issued = issued;
+    } else if (warp < hpc) {
         // ------------------------------ consumers -----------------------------
+        const int gh = hgrp * hpc + warp;                     // this warp's KV head
+        const int h0 = gh * p.group + tile * kRowsPerTile;    // its first query head
         const int r = lane >> 2, q4 = lane & 3;
-        // Q fragments (A operand, rows = query heads of this tile), held for the CTA's lifetime
         uint32_t qa[D / 16][4];
         {
-            const int h0 = g * p.group + tile * kRowsPerTile;
             const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
                 static_cast<const __nv_bfloat16 *>(p.query) +
                 (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D);
@@ -158,31 +432,31 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         const float sl2 = p.scale_log2;
 
-        for (int i = warp; i < ntiles; i += C::kConsumerWarps) {
+        for (int i = 0; i < ntiles; ++i) {
             if (*reinterpret_cast<volatile int *>(&s_abort)) break;
-            const int s = i % kStages, k = i / kStages;
+            const int s = i % nstages, k = i / nstages;
             if (!mbar_wait(smem_addr(&bars[s]), k & 1)) {
                 record_status(p.status, kStatusTimeout);
                 s_abort = 1;
                 break;
             }
-            unsigned char *stage = smem + s * C::kStageBytes;
-            const uint32_t kbase = smem_addr(stage);
-            const uint32_t vbase = kbase + C::kTileBytes;
-            const int t0 = (w.blk_begin + i) * BS;
-            const int valid = min(BS, w.len - t0);
-            if (valid < BS) {
-                // zero V rows past the context (whole 128-byte rows: swizzle is irrelevant)
-                uint4 *vz = reinterpret_cast<uint4 *>(stage + C::kTileBytes);
-                for (int c = lane; c < C::kHalves * BS * 8; c += 32)
-                    if ((c % (BS * 8)) / 8 >= valid) vz[c] = make_uint4(0u, 0u, 0u, 0u);
+            unsigned char *kst = smem + s * stage_bytes + warp * C::kHeadBytes;
+            const uint32_t kbase = smem_addr(kst);
+            const uint32_t vbase = kbase + v_off;
+            const int valid = min(TT, tok_end - (tok_begin + i * TT));
+            if (valid < TT) {
+                // zero this head's V rows past the context (whole 128-byte rows)
+                uint4 *vz = reinterpret_cast<uint4 *>(kst + v_off);
+                for (int c = lane; c < C::kHalves * TT * 8; c += 32)
+                    if ((c % (TT * 8)) / 8 >= valid) vz[c] = make_uint4(0u, 0u, 0u, 0u);
                 __syncwarp();
             }
 
-            // ---- S = Q K^T ----
+            // ---- S = Q K^T (two interleaved accumulator chains per n-tile) ----
             float sacc[kNT][4];
 #pragma unroll
             for (int j = 0; j < kNT; ++j) {
+                float acc2[4] = {0.f, 0.f, 0.f, 0.f};
                 sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; kk += 2) {
@@ -193,74 +467,81 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(addr, b0, b1, b2, b3);
                     mma_bf16_16816(sacc[j], qa[kk], b0, b1);
-                    mma_bf16_16816(sacc[j], qa[kk + 1], b2, b3);
+                    mma_bf16_16816(acc2, qa[kk + 1], b2, b3);
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[j][e] = (sacc[j][e] + acc2[e]) * sl2;
             }
 
             // ---- online softmax (base 2) ----
+            if (valid < TT) {
+#pragma unroll
+                for (int j = 0; j < kNT; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (8 * j + 2 * q4 + e >= valid) sacc[j][e] = sacc[j][2 + e] = -INFINITY;
+            }
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < kNT; ++j)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const bool live = 8 * j + 2 * q4 + e < valid;
-                    const float s0 = live ? sacc[j][e] * sl2 : -INFINITY;
-                    const float s1 = live ? sacc[j][2 + e] * sl2 : -INFINITY;
-                    sacc[j][e] = s0;
-                    sacc[j][2 + e] = s1;
-                    mx0 = fmaxf(mx0, s0);
-                    mx1 = fmaxf(mx1, s1);
-                }
+            for (int j = 0; j < kNT; ++j) {
+                mx0 = fmaxf(mx0, fmaxf(sacc[j][0], sacc[j][1]));
+                mx1 = fmaxf(mx1, fmaxf(sacc[j][2], sacc[j][3]));
+            }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            l0 *= a0;
-            l1 *= a1;
+            st.t0 = fmaxf(st.t0, mx0);
+            st.t1 = fmaxf(st.t1, mx1);
+            // Lazy rescale: the reference max only moves when a score exceeds it
+            // by more than kRescaleSlack (base 2), so 2^(s - m) stays <= 2^slack
+            // and the O rescale is skipped while no row in the warp needs it.
+            const bool need0 = mx0 > st.m0 + kRescaleSlack, need1 = mx1 > st.m1 + kRescaleSlack;
+            if (__any_sync(0xffffffffu, need0 || need1)) {
+                const float mn0 = need0 ? fmaxf(st.m0, mx0) : st.m0;
+                const float mn1 = need1 ? fmaxf(st.m1, mx1) : st.m1;
+                const float a0 = fast_exp2(st.m0 - mn0), a1 = fast_exp2(st.m1 - mn1);
+                st.m0 = mn0;
+                st.m1 = mn1;
+                st.l0 *= a0;
+                st.l1 *= a1;
 #pragma unroll
-            for (int i2 = 0; i2 < D / 8; ++i2) {
-                o[i2][0] *= a0;
-                o[i2][1] *= a0;
-                o[i2][2] *= a1;
-                o[i2][3] *= a1;
+                for (int i2 = 0; i2 < D / 8; ++i2) {
+                    st.o[i2][0] *= a0;
+                    st.o[i2][1] *= a0;
+                    st.o[i2][2] *= a1;
+                    st.o[i2][3] *= a1;
+                }
             }
-            constexpr int kKS = (kNT + 1) / 2;  // 16-token k-steps of P.V
-            uint32_t phi[kKS][4], plo[kKS][4];
-#pragma unroll
-            for (int u = 0; u < kKS; ++u) phi[u][2] = phi[u][3] = plo[u][2] = plo[u][3] = 0u;
+            const float mn0 = st.m0, mn1 = st.m1;
+            uint32_t phi[4], plo[4];
+            phi[2] = phi[3] = plo[2] = plo[3] = 0u;
 #pragma unroll
             for (int j = 0; j < kNT; ++j) {
                 const float p0 = fast_exp2(sacc[j][0] - mn0), p1 = fast_exp2(sacc[j][1] - mn0);
                 const float p2 = fast_exp2(sacc[j][2] - mn1), p3 = fast_exp2(sacc[j][3] - mn1);
-                l0 += p0 + p1;
-                l1 += p2 + p3;
-                const int u = j >> 1, hh = (j & 1) * 2;
-                split_bf16x2(p0, p1, phi[u][hh], plo[u][hh]);
-                split_bf16x2(p2, p3, phi[u][hh + 1], plo[u][hh + 1]);
+                st.l0 += p0 + p1;
+                st.l1 += p2 + p3;
+                split_bf16x2(p0, p1, phi[2 * j], plo[2 * j]);
+                split_bf16x2(p2, p3, phi[2 * j + 1], plo[2 * j + 1]);
             }
 
             // ---- O += P V ----
-            if constexpr (BS >= 16) {
+            if constexpr (TT == 16) {
 #pragma unroll
-                for (int u = 0; u < kKS; ++u)
-#pragma unroll
-                    for (int dn = 0; dn < D / 8; dn += 2) {
-                        const int mi = lane >> 3;
-                        const int tok = 16 * u + (mi & 1) * 8 + (lane & 7);
-                        const int c = dn + (mi >> 1);
-                        const uint32_t addr = vbase + (c >> 3) * C::kHalfBytes + tok * 128 +
-                                              (((c & 7) ^ (tok & 7)) << 4);
-                        uint32_t v0, v1, v2, v3;
-                        ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-                        mma_bf16_16816(o[dn], phi[u], v0, v1);
-                        mma_bf16_16816(o[dn + 1], phi[u], v2, v3);
-                        mma_bf16_16816(o[dn], plo[u], v0, v1);
-                        mma_bf16_16816(o[dn + 1], plo[u], v2, v3);
-                    }
+                for (int dn = 0; dn < D / 8; dn += 2) {
+                    const int mi = lane >> 3;
+                    const int tok = (mi & 1) * 8 + (lane & 7);
+                    const int c = dn + (mi >> 1);
+                    const uint32_t addr = vbase + (c >> 3) * C::kHalfBytes + tok * 128 +
+                                          (((c & 7) ^ (tok & 7)) << 4);
+                    uint32_t v0, v1, v2, v3;
+                    ldmatrix_x4_trans(addr, v0, v1, v2, v3);
+                    mma_bf16_16816(st.o[dn], phi, v0, v1);
+                    mma_bf16_16816(st.o[dn + 1], phi, v2, v3);
+                    mma_bf16_16816(st.o[dn], plo, v0, v1);
+                    mma_bf16_16816(st.o[dn + 1], plo, v2, v3);
+                }
             } else {
 #pragma unroll
                 for (int dn = 0; dn < D / 8; dn += 4) {
@@ -270,88 +551,101 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                           (((c & 7) ^ (tok & 7)) << 4);
                     uint32_t v0, v1, v2, v3;
                     ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-                    mma_bf16_16816(o[dn], phi[0], v0, 0u);
-                    mma_bf16_16816(o[dn + 1], phi[0], v1, 0u);
-                    mma_bf16_16816(o[dn + 2], phi[0], v2, 0u);
-                    mma_bf16_16816(o[dn + 3], phi[0], v3, 0u);
-                    mma_bf16_16816(o[dn], plo[0], v0, 0u);
-                    mma_bf16_16816(o[dn + 1], plo[0], v1, 0u);
-                    mma_bf16_16816(o[dn + 2], plo[0], v2, 0u);
-                    mma_bf16_16816(o[dn + 3], plo[0], v3, 0u);
+                    mma_bf16_16816(st.o[dn], phi, v0, 0u);
+                    mma_bf16_16816(st.o[dn + 1], phi, v1, 0u);
+                    mma_bf16_16816(st.o[dn + 2], phi, v2, 0u);
+                    mma_bf16_16816(st.o[dn + 3], phi, v3, 0u);
+                    mma_bf16_16816(st.o[dn], plo, v0, 0u);
+                    mma_bf16_16816(st.o[dn + 1], plo, v1, 0u);
+                    mma_bf16_16816(st.o[dn + 2], plo, v2, 0u);
+                    mma_bf16_16816(st.o[dn + 3], plo, v3, 0u);
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bars[kStages + s]));
+            if (lane == 0) mbar_arrive(smem_addr(&bars[C::kMaxStages + s]));
         }
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 1);
+        st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 2);
+        st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
+        st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
+        if (!cluster) warp_epilogue<D>(p, st, b, gh, tile, part, h0, rows, w.nparts, lane);
     }
-    __syncthreads();
 
     // Drain: wait (bounded) for the last phase of every stage this CTA armed,
-    // so that no copy is still landing in shared memory we are about to reuse.
+    // so that no copy is still landing in shared memory when the CTA exits
+    // (or when the ring is reused below).
+    __syncthreads();
     if (threadIdx.x == 0) {
         const int issued = s_issued;
-        for (int s = 0; s < kStages && s < issued; ++s) {
-            const int k_last = (issued - 1 - s) / kStages;
+        for (int s = 0; s < nstages && s < issued; ++s) {
+            const int k_last = (issued - 1 - s) / nstages;
             if (!mbar_wait(smem_addr(&bars[s]), k_last & 1)) record_status(p.status, kStatusTimeout);
         }
     }
-    __syncthreads();
-
-    // Per-warp softmax states -> shared memory, then merged across warps.
-    float *mbase = reinterpret_cast<float *>(smem);
-    using L = MergeLayout<D>;
-    if (warp < C::kConsumerWarps) {
-        const int r = lane >> 2, q4 = lane & 3;
-        float *wo = L::o(mbase, warp);
-#pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn) {
-            const int d = 8 * dn + 2 * q4;
-            *reinterpret_cast<float2 *>(&wo[r * L::kStride + d]) = make_float2(o[dn][0], o[dn][1]);
-            *reinterpret_cast<float2 *>(&wo[(r + 8) * L::kStride + d]) = make_float2(o[dn][2], o[dn][3]);
-        }
-        if (q4 == 0) {
-            L::m(mbase, warp)[r] = m0;
-            L::m(mbase, warp)[r + 8] = m1;
-            L::l(mbase, warp)[r] = l0;
-            L::l(mbase, warp)[r + 8] = l1;
-        }
+    if (cluster) {
+        __syncthreads();
+        cluster_exchange_merge<D>(p, st, reinterpret_cast<float *>(smem), b, hgrp, tile, rows, warp, lane);
     }
-    __syncthreads();
-    combine_warps<D>(mbase, C::kConsumerWarps, rows);
-    write_result<D>(p, mbase, C::kConsumerWarps, b, g, tile, part, rows, w.nparts);
 }
 
-template <int D, int BS>
+template <int D, int TT>
 static cudaError_t launch_impl(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                dim3 grid, cudaStream_t stream) {
-    using C = MmaCfg<D, BS>;
-    auto kern = decode_mma_kernel<D, BS>;
+    using C = MmaCfg<D, TT>;
+    auto kern = decode_mma_kernel<D, TT>;
     static unsigned long long done = 0;
-    cudaError_t e = ensure_smem_limit(kern, C::kSmemBytes, done);
+    cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    if (!p.cluster_merge) {
+        kern<<<grid, 32 * (p.heads_per_cta + 1), C::smem_bytes(p.ring_bytes), stream>>>(tk, tv, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(32 * (p.heads_per_cta + 1));
+    cfg.dynamicSmemBytes = C::smem_bytes(p.ring_bytes);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = grid.x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 bool decode_mma_supported(int head_dim, int block_size) {
     return (head_dim == 64 || head_dim == 128) &&
-           (block_size == 8 || block_size == 16 || block_size == 32);
+           (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64 ||
+            block_size == 128 || block_size == 256);
+}
+
+int decode_mma_tile_tokens(int block_size) { return block_size < 16 ? block_size : 16; }
+
+int decode_mma_heads_per_cta(int num_kv_heads, int max_heads) {
+    for (int h = max_heads < MmaCfg<128, 16>::kMaxHeads ? max_heads : MmaCfg<128, 16>::kMaxHeads; h > 1; --h)
+        if (num_kv_heads % h == 0) return h;
+    return 1;
+}
+
+int decode_mma_stage_bytes(int head_dim, int block_size, int heads_per_cta) {
+    return 2 * heads_per_cta * decode_mma_tile_tokens(block_size) * head_dim * 2;
+}
+
+int decode_mma_cluster_bytes(int head_dim, int heads_per_cta) {
+    return heads_per_cta * (32 + kRowsPerTile * head_dim) * 4;
 }
 
 cudaError_t launch_decode_mma(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                               dim3 grid, cudaStream_t stream) {
+    const int tt = decode_mma_tile_tokens(p.block_size);
     if (p.head_dim == 128) {
-        if (p.block_size == 16) return launch_impl<128, 16>(p, tk, tv, grid, stream);
-        if (p.block_size == 32) return launch_impl<128, 32>(p, tk, tv, grid, stream);
-        if (p.block_size == 8) return launch_impl<128, 8>(p, tk, tv, grid, stream);
+        if (tt == 16) return launch_impl<128, 16>(p, tk, tv, grid, stream);
+        if (tt == 8) return launch_impl<128, 8>(p, tk, tv, grid, stream);
     } else if (p.head_dim == 64) {
-        if (p.block_size == 16) return launch_impl<64, 16>(p, tk, tv, grid, stream);
-        if (p.block_size == 32) return launch_impl<64, 32>(p, tk, tv, grid, stream);
-        if (p.block_size == 8) return launch_impl<64, 8>(p, tk, tv, grid, stream);
+        if (tt == 16) return launch_impl<64, 16>(p, tk, tv, grid, stream);
+        if (tt == 8) return launch_impl<64, 8>(p, tk, tv, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

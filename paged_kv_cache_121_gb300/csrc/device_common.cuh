@@ -12,7 +12,7 @@
 namespace pa {
 
 constexpr int kRowsPerTile = 16;     // query heads per CTA (the MMA's M)
-constexpr int kMaxSplits = 256;      // bound on fused partitions (merge weights live in smem)
+constexpr int kMaxSplits = 64;       // bound on fused partitions (the merge keeps two per lane)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far above any legal wait
@@ -39,6 +39,10 @@ struct DecodeParams {
     int max_blocks, num_blocks;
     int group;           // num_heads / num_kv_heads
     int ntile;           // cdiv(group, 16)
+    int heads_per_cta;   // KV heads one CTA serves (grid.y = Hkv / heads_per_cta * ntile)
+    int ring_bytes;      // shared-memory ring of the tensor-core kernel
+    int cluster_merge;   // fused split merged through distributed shared memory
+                         // (grid.x = nsplit = cluster size)
     int nsplit;          // grid.x: partitions per (sequence, head tile)
     int part_blocks;     // blocks per partition
     int mode;
@@ -153,6 +157,39 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
         "l"(policy)
         : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// thread-block cluster: rank, peer shared-memory addresses, barrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local_smem_addr, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_smem_addr), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
+// All threads of every CTA of the cluster: writes before it are visible to
+// reads after it, cluster-wide.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -369,6 +406,28 @@ __device__ void write_result(const DecodeParams &p, float *base, int nwarps, int
         store_out(p, (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + d, acc * s_inv[r]);
     }
     if (threadIdx.x == 0) *counter = 0u;  // ready for the next call
+}
+
+// One warp, one KV head: rows h0 .. h0+rows-1 of a partition holding no tokens.
+template <int D>
+__device__ void warp_write_empty(const DecodeParams &p, int b, int h0, int part, int rows, int nparts,
+                                 int lane) {
+    if (p.mode == kModeSplitK) {
+        const int P = p.nsplit;
+        for (int r = 0; r < rows; ++r) {
+            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * P + part;
+            for (int d = lane; d < D; d += 32) p.tmp_out[row * D + d] = 0.f;
+            if (lane == 0) {
+                p.max_logits[row] = -INFINITY;
+                p.exp_sums[row] = 0.f;
+            }
+        }
+        return;
+    }
+    if (nparts == 0 && part == 0)
+        for (int r = 0; r < rows; ++r)
+            for (int d = lane; d < D; d += 32)
+                store_out(p, (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + d, 0.f);
 }
 
 // A CTA whose partition holds no tokens.

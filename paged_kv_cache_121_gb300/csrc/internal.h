@@ -10,6 +10,11 @@ namespace pa {
 struct DecodeParams;
 
 bool decode_mma_supported(int head_dim, int block_size);
+int decode_mma_tile_tokens(int block_size);       // tokens per TMA tile / pipeline stage
+int decode_mma_heads_per_cta(int num_kv_heads, int max_heads);   // KV heads (consumer warps) per CTA
+int decode_mma_stage_bytes(int head_dim, int block_size, int heads_per_cta);
+int decode_mma_cluster_bytes(int head_dim, int heads_per_cta);   // shared memory the cluster merge needs
+constexpr int kMaxClusterSplits = 8;                              // portable cluster size
 cudaError_t launch_decode_mma(const DecodeParams &p, const CUtensorMap &tmap_k,
                               const CUtensorMap &tmap_v, dim3 grid, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, cudaStream_t stream);

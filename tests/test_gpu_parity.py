@@ -38,6 +38,9 @@ SMALL = [
     ((19, 90), 8, 2, 128, 4, True),                # block size outside the tensor-core set
     ((19, 90), 8, 2, 64, 64, True),
     ((10, 45), 6, 3, 64, 16, False),
+    ((33, 200, 17), 24, 12, 128, 16, True),        # 12 KV heads: groups of 6 per CTA
+    ((70, 300), 32, 16, 64, 32, True),             # 16 KV heads: two groups of 8
+    ((5, 600), 12, 3, 128, 128, True),             # large blocks: 8 tiles per block
 ]
 
 

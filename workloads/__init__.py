@@ -211,11 +211,13 @@ LONG_TOKENS = 32768
 LONG_POOL_TOKENS = 9000 * 16   # the pool holds 144,000 tokens at any block size
 
 
-def long_context(block_size: int = 16, num_seqs: int = 4) -> DecodeBatch:
+def long_context(block_size: int = 16, num_seqs: int = 4, copies: int = 1) -> DecodeBatch:
     """4 sequences of 32,768 tokens, Hq 64, Hkv 8, D 128, bf16, pool of
-    144,000 tokens (9,000 blocks at 16)."""
-    lens = np.full(num_seqs, LONG_TOKENS, dtype=np.int32)
-    return make_batch("long", lens, 64, 8, 128, block_size, LONG_POOL_TOKENS // block_size, bf16=True)
+    144,000 tokens (9,000 blocks at 16). ``copies`` > 1 draws several disjoint
+    batches, each with its own 144,000-token share of the pool."""
+    lens = np.full(num_seqs * copies, LONG_TOKENS, dtype=np.int32)
+    return make_batch("long", lens, 64, 8, 128, block_size,
+                      copies * LONG_POOL_TOKENS // block_size, bf16=True)
 
 
 @dataclasses.dataclass

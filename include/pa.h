@@ -146,6 +146,37 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
                            size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Decode for callers that cannot allocate device memory. (The source pages
+ * have no counterpart: this is a library convenience.)
+ *
+ * Some callers cannot provide the scratch pa_decode may need: an engine whose
+ * device memory is reserved up front by another allocator (cudaMalloc would
+ * fail there or bypass its accounting), or a plugin interface that passes only
+ * the operation's inputs and outputs. This entry point computes what pa_decode
+ * computes, with the same arguments minus the workspace, and merges a context
+ * split through a fixed scratch array built into the library:
+ * PA_STATIC_SCRATCH_BYTES bytes of device memory that every GPU loading the
+ * library holds until the process exits. It allocates nothing.
+ *  - A problem whose split needs more scratch than that returns
+ *    PA_ERR_WORKSPACE before anything is launched (use pa_decode with a
+ *    workspace of pa_decode_workspace_size() bytes instead).
+ *  - The first call on a device looks up the scratch's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call shares the one scratch array and its arrival counters are
+ *    cleared on `stream` at each call: calls that overlap on the GPU (other
+ *    streams, other threads) race and give wrong results. Serialise them.
+ * ---------------------------------------------------------------------- */
+#define PA_STATIC_SCRATCH_BYTES (8u << 20)
+PA_API pa_status pa_decode_static_scratch(void *out, pa_dtype out_dtype, const void *query,
+                                          pa_dtype q_dtype, const void *k_cache,
+                                          const void *v_cache, pa_dtype kv_dtype,
+                                          const int32_t *block_tables,
+                                          const int32_t *context_lens, int num_seqs,
+                                          int num_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int max_blocks_per_seq, int num_blocks,
+                                          int max_context_len, float scale, void *stream);
+
+/* ------------------------------------------------------------------------
  * Split-K decode: attention over fixed partitions of partition_size tokens
  * (a multiple of block_size), to be combined by pa_lse_merge. The pages
  * describe no split; its definition is the plain one: partition p of

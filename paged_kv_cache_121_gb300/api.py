@@ -105,6 +105,20 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, max_cont
                                 _stream(stream)), "pa_decode")
 
 
+def pa_decode_static_scratch(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                             scale, stream=None) -> None:
+    """pa_decode without a workspace argument: a context split is merged
+    through the library's own fixed scratch (for callers that cannot
+    allocate device memory; calls must not overlap on the GPU)."""
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    B, hq, _ = (int(x) for x in query.shape)
+    _check(_lib.load().pa_decode_static_scratch(
+        _ptr(out), _dtype(out), _ptr(query), _dtype(query), _ptr(k_cache), _ptr(v_cache),
+        _dtype(k_cache), _ptr(block_tables), _ptr(context_lens), B, hq, hkv, d, bs,
+        int(block_tables.shape[1]), nb, int(max_context_len), float(scale), _stream(stream)),
+        "pa_decode_static_scratch")
+
+
 def pa_decode_splitk(tmp_out, max_logits, exp_sums, partition_size, query, k_cache, v_cache,
                      block_tables, context_lens, max_context_len, scale, stream=None) -> None:
     """Per-partition attention: tmp_out [B, Hq, P, D], max_logits / exp_sums [B, Hq, P] (float32)."""

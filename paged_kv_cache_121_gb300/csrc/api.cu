@@ -267,6 +267,54 @@ void fill_common(DecodeParams &p, const DecodeShape &s, const void *query, pa_dt
 }
 
 }  // namespace
+
+int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes, void *stream) {
+    const DecodeShape s{c.num_seqs, c.num_heads, c.num_kv_heads, c.head_dim, c.block_size,
+                        c.max_blocks_per_seq, c.num_blocks, c.max_context_len};
+    const pa_dtype out_dtype = static_cast<pa_dtype>(c.out_dtype);
+    const pa_dtype q_dtype = static_cast<pa_dtype>(c.q_dtype);
+    const pa_dtype kv_dtype = static_cast<pa_dtype>(c.kv_dtype);
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    if (!valid_dtype(out_dtype) || !std::isfinite(c.scale)) return PA_ERR_INVALID_ARG;
+    if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
+    if (c.num_seqs == 0) return PA_OK;
+    int dev;
+    if ((st = current_device(&dev)) != PA_OK) return st;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PA_ERR_CUDA;
+    Plan pl = plan_split(s, sms, use_mma(s, kv_dtype == PA_BF16));
+    pl.cluster = false;   // the split, if any, goes through the scratch
+    const WorkspaceLayout wl = workspace_layout(s, pl);
+    if (pl.nsplit > 1 && (wl.total > scratch_bytes || !scratch || !aligned16(scratch)))
+        return PA_ERR_WORKSPACE;
+    if (!c.out || !c.query || !c.k_cache || !c.v_cache || !c.block_tables || !c.context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(c.out) || !aligned16(c.query) || !aligned16(c.k_cache) || !aligned16(c.v_cache))
+        return PA_ERR_INVALID_ARG;
+    DecodeParams p;
+    fill_common(p, s, c.query, q_dtype, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale);
+    p.out = c.out;
+    p.out_bf16 = out_dtype == PA_BF16;
+    p.ntile = pl.ntile;
+    p.heads_per_cta = pl.heads_per_cta;
+    p.nsplit = pl.nsplit;
+    p.part_blocks = pl.part_blocks;
+    p.cluster_merge = 0;
+    if (pl.nsplit > 1) {
+        char *ws = static_cast<char *>(scratch);
+        p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+        p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+        p.ws_count = reinterpret_cast<unsigned *>(ws + wl.count_off);
+        p.mode = kModeFused;
+        if (cudaMemsetAsync(p.ws_count, 0, wl.total - wl.count_off, as_stream(stream)) != cudaSuccess)
+            return PA_ERR_CUDA;
+    } else {
+        p.mode = kModeFinal;
+    }
+    return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
+}
+
 }  // namespace pa
 
 using namespace pa;

@@ -25,6 +25,29 @@ cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, cons
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
                                      void *v_cache, const int64_t *slot_mapping, int num_tokens,
                                      int64_t num_slots, int row_bytes, cudaStream_t stream);
+// Arguments of a decode call (mirrors pa_decode, dtypes as pa_dtype values).
+struct DecodeCall {
+    void *out;
+    int out_dtype;
+    const void *query;
+    int q_dtype;
+    const void *k_cache;
+    const void *v_cache;
+    int kv_dtype;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    int num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+        max_context_len;
+    float scale;
+};
+
+// Decode whose context split (when the plan splits) is always merged through
+// `scratch` (never inside a cluster). The arrival counters in the scratch are
+// cleared on `stream` before the launch. Returns a pa_status value;
+// PA_ERR_WORKSPACE (checked before any pointer) when the plan needs more
+// than scratch_bytes.
+int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes, void *stream);
+
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
                                int num_pairs, int64_t num_blocks, int64_t block_bytes,
                                cudaStream_t stream);

@@ -197,16 +197,39 @@ struct WorkspaceLayout {
     size_t o_off, ml_off, count_off, total;
 };
 
+// Wide splits are written in split-K form (normalised partial outputs,
+// maxima, sums) and merged by the log-sum-exp merge kernel.
 WorkspaceLayout workspace_layout(const DecodeShape &s, const Plan &pl) {
     WorkspaceLayout w{};
     if (pl.nsplit <= 1 || pl.cluster) return w;
     const size_t rows = static_cast<size_t>(s.num_seqs) * s.num_heads * pl.nsplit;
     w.o_off = 0;
-    w.ml_off = align256(rows * s.head_dim * sizeof(float));
-    w.count_off = w.ml_off + align256(rows * 2 * sizeof(float));
-    w.total = w.count_off +
-              align256(static_cast<size_t>(s.num_seqs) * s.num_kv_heads * pl.ntile * sizeof(unsigned));
+    w.ml_off = align256(rows * s.head_dim * sizeof(float));            // maxima
+    w.count_off = w.ml_off + align256(rows * sizeof(float));            // sums
+    w.total = w.count_off + align256(rows * sizeof(float));
     return w;
+}
+
+pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, int dev,
+                        cudaStream_t stream);
+
+// Decode of a wide split: partitions in split-K form into the workspace, then
+// the merge kernel on the same stream.
+pa_status launch_split_and_merge(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, int dev,
+                                 void *workspace, const WorkspaceLayout &wl, void *out, bool out_bf16,
+                                 cudaStream_t stream) {
+    char *ws = static_cast<char *>(workspace);
+    p.tmp_out = reinterpret_cast<float *>(ws + wl.o_off);
+    p.max_logits = reinterpret_cast<float *>(ws + wl.ml_off);
+    p.exp_sums = reinterpret_cast<float *>(ws + wl.count_off);
+    p.mode = kModeSplitK;
+    p.cluster_merge = 0;
+    pa_status st = launch_decode(s, p, kv_dtype, dev, stream);
+    if (st != PA_OK) return st;
+    const cudaError_t e = launch_lse_merge(out, out_bf16 ? 1 : 0, p.tmp_out, p.max_logits, p.exp_sums,
+                                           p.context_lens, s.num_seqs, s.num_heads, s.head_dim,
+                                           p.nsplit, p.part_blocks * s.block_size, stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status check_dtypes(pa_dtype q_dtype, pa_dtype kv_dtype) {
@@ -301,17 +324,10 @@ int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes
     p.nsplit = pl.nsplit;
     p.part_blocks = pl.part_blocks;
     p.cluster_merge = 0;
-    if (pl.nsplit > 1) {
-        char *ws = static_cast<char *>(scratch);
-        p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-        p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
-        p.ws_count = reinterpret_cast<unsigned *>(ws + wl.count_off);
-        p.mode = kModeFused;
-        if (cudaMemsetAsync(p.ws_count, 0, wl.total - wl.count_off, as_stream(stream)) != cudaSuccess)
-            return PA_ERR_CUDA;
-    } else {
-        p.mode = kModeFinal;
-    }
+    if (pl.nsplit > 1)
+        return launch_split_and_merge(s, p, kv_dtype, dev, scratch, wl, c.out, out_dtype == PA_BF16,
+                                      as_stream(stream));
+    p.mode = kModeFinal;
     return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
 }
 
@@ -439,11 +455,8 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
     } else if (pl.nsplit > 1) {
         const WorkspaceLayout wl = workspace_layout(s, pl);
         if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-        char *ws = static_cast<char *>(workspace);
-        p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-        p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
-        p.ws_count = reinterpret_cast<unsigned *>(ws + wl.count_off);
-        p.mode = kModeFused;
+        return launch_split_and_merge(s, p, kv_dtype, dev, workspace, wl, out, out_dtype == PA_BF16,
+                                      as_stream(stream));
     } else {
         p.mode = kModeFinal;
     }

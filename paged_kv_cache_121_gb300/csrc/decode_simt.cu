@@ -209,11 +209,11 @@ lse_merge_kernel(void *out, int out_bf16, const float *tmp_out, const float *max
     __syncthreads();
     const float inv = s_inv;
     for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
+        // partitions below np all hold tokens; independent loads, unrolled
         float acc = 0.f;
-        for (int q = 0; q < np; ++q) {
-            const float wq = wgt[q];
-            if (wq != 0.f) acc += wq * tmp_out[(row0 + q) * head_dim + d];
-        }
+        const float *src = tmp_out + row0 * head_dim + d;
+#pragma unroll 8
+        for (int q = 0; q < np; ++q) acc += wgt[q] * __ldcg(src + static_cast<int64_t>(q) * head_dim);
         const int64_t oi = (static_cast<int64_t>(b) * num_heads + h) * head_dim + d;
         if (out_bf16)
             reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(acc * inv);

@@ -301,7 +301,7 @@ __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, co
     cluster_sync_all();   // peers have finished reading this CTA's shared memory
 }
 
-template <int D, int TT>
+template <int D, int TT, bool kCluster>
 __global__ void __launch_bounds__(MmaCfg<D, TT>::kThreads, 1)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
@@ -323,7 +323,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int rows = min(kRowsPerTile, p.group - tile * kRowsPerTile);
     const SeqWork w = seq_work(p, b, part);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool cluster = p.cluster_merge != 0;
+    // (one instantiation per epilogue keeps the other's registers out of the loop)
+    constexpr bool cluster = kCluster;
     if (w.blk_begin >= w.blk_end && !cluster) {
         if (warp < hpc) {
             const int gh = hgrp * hpc + warp;
@@ -592,18 +593,23 @@ template <int D, int TT>
 static cudaError_t launch_impl(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                dim3 grid, cudaStream_t stream) {
     using C = MmaCfg<D, TT>;
-    auto kern = decode_mma_kernel<D, TT>;
+    const size_t smem = C::smem_bytes(p.ring_bytes);
+    if (!p.cluster_merge) {
+        auto kern = decode_mma_kernel<D, TT, false>;
+        static unsigned long long done = 0;
+        cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, 32 * (p.heads_per_cta + 1), smem, stream>>>(tk, tv, p);
+        return cudaGetLastError();
+    }
+    auto kern = decode_mma_kernel<D, TT, true>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
     if (e != cudaSuccess) return e;
-    if (!p.cluster_merge) {
-        kern<<<grid, 32 * (p.heads_per_cta + 1), C::smem_bytes(p.ring_bytes), stream>>>(tk, tv, p);
-        return cudaGetLastError();
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(32 * (p.heads_per_cta + 1));
-    cfg.dynamicSmemBytes = C::smem_bytes(p.ring_bytes);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

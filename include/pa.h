@@ -124,15 +124,18 @@ PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *blo
  *   max_context_len  host-side upper bound of context_lens (sizes the grid;
  *                tokens past it are not attended).
  *   scale        multiplies q.k (normally 1/sqrt(head_dim)).
- *   workspace    scratch for the context split: NULL / 0 bytes runs one
- *                CTA per (sequence, KV head); otherwise at least
- *                pa_decode_workspace_size() bytes, ZERO-FILLED before the
- *                first call. The kernel leaves it ready for the next call
- *                (its counters return to zero). Calls that share a
+ *   workspace    scratch for a wide context split: at least
+ *                pa_decode_workspace_size() bytes (0 when the plan needs
+ *                none), or NULL / 0 bytes. Splits of up to 8 partitions are
+ *                merged inside a thread-block cluster and need no workspace;
+ *                wider ones need it (without it the split is capped at 8,
+ *                or, on the CUDA-core kernel, not split at all). Its
+ *                contents need no initialisation. Calls that share a
  *                workspace must not overlap on the GPU.
  *   Supported: head_dim 64 or 128; num_heads % num_kv_heads == 0;
  *   (q, kv) dtypes (F32, F32) or (BF16, BF16); block_size 1..256.
- *   bf16 caches with block_size 8, 16 or 32 run the tensor-core kernel.
+ *   bf16 caches with block_size 8, 16, 32, 64, 128 or 256 run the
+ *   tensor-core kernel, the rest the CUDA-core kernel.
  * ---------------------------------------------------------------------- */
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                        int head_dim, int block_size, int max_context_len);

@@ -248,55 +248,64 @@ __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, co
             *reinterpret_cast<float2 *>(reg + 32 + r * D + d) = make_float2(st.o[dn][0], st.o[dn][1]);
             *reinterpret_cast<float2 *>(reg + 32 + (r + 8) * D + d) = make_float2(st.o[dn][2], st.o[dn][3]);
         }
-        if (q4 == 0) {
-            reg[r] = st.m0;
-            reg[r + 8] = st.m1;
-            reg[16 + r] = st.l0;
-            reg[16 + r + 8] = st.l1;
+        if (q4 == 0) {   // (max, sum) pairs, row-major
+            *reinterpret_cast<float2 *>(reg + 2 * r) = make_float2(st.m0, st.l0);
+            *reinterpret_cast<float2 *>(reg + 2 * (r + 8)) = make_float2(st.m1, st.l1);
         }
     }
     cluster_sync_all();   // every partition's state is now readable cluster-wide
 
+    // Each thread merges 4 consecutive dims of one (head, row): it issues the
+    // reads of all partitions (a 16-byte vector of O and the (max, sum) pair
+    // each) before using any of them, so the exchange costs one round of
+    // distributed-shared-memory reads.
     const int ns = p.nsplit;                 // cluster size
     const int rank = static_cast<int>(cluster_rank());
-    const int total = hpc * rows * D;
+    constexpr int kD4 = D / 4;
+    const int total = hpc * rows * kD4;
     const int chunk = (total + ns - 1) / ns;
     const int begin = rank * chunk;
     const int end = min(total, begin + chunk);
     const uint32_t base = smem_addr(sm);
     for (int idx = begin + static_cast<int>(threadIdx.x); idx < end; idx += blockDim.x) {
-        const int j = idx / (rows * D);
-        const int rem = idx - j * rows * D;
-        const int rr = rem / D, d = rem - rr * D;
-        const uint32_t ml_off = base + 4u * static_cast<uint32_t>(j * kRegion + rr);
-        const uint32_t o_off = base + 4u * static_cast<uint32_t>(j * kRegion + 32 + rr * D + d);
-        float mq[8], lq[8], oq[8];
+        const int j = idx / (rows * kD4);
+        const int rem = idx - j * rows * kD4;
+        const int rr = rem / kD4, d4 = rem - rr * kD4;
+        const uint32_t ml_off = base + 4u * static_cast<uint32_t>(j * kRegion + 2 * rr);
+        const uint32_t o_off = base + 4u * static_cast<uint32_t>(j * kRegion + 32 + rr * D + 4 * d4);
+        float2 ml[8];
+        float4 oq[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             if (q < ns) {
-                mq[q] = ld_cluster_f32(cluster_map(ml_off, q));
-                lq[q] = ld_cluster_f32(cluster_map(ml_off + 64u, q));
-                oq[q] = ld_cluster_f32(cluster_map(o_off, q));
+                ml[q] = ld_cluster_f32x2(cluster_map(ml_off, q));
+                oq[q] = ld_cluster_f32x4(cluster_map(o_off, q));
             } else {
-                mq[q] = -INFINITY;
-                lq[q] = 0.f;
-                oq[q] = 0.f;
+                ml[q] = make_float2(-INFINITY, 0.f);
+                oq[q] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         float M = -INFINITY;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            if (lq[q] > 0.f) M = fmaxf(M, mq[q]);
-        float L = 0.f, acc = 0.f;
+            if (ml[q].y > 0.f) M = fmaxf(M, ml[q].x);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            if (lq[q] > 0.f) {
-                const float wq = fast_exp2(mq[q] - M);
-                L += wq * lq[q];
-                acc += wq * oq[q];
+            if (ml[q].y > 0.f) {
+                const float wq = fast_exp2(ml[q].x - M);
+                L += wq * ml[q].y;
+                acc.x += wq * oq[q].x;
+                acc.y += wq * oq[q].y;
+                acc.z += wq * oq[q].z;
+                acc.w += wq * oq[q].w;
             }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
         const int h = (hgrp * hpc + j) * p.group + tile * kRowsPerTile + rr;
-        store_out(p, (static_cast<int64_t>(b) * p.num_heads + h) * D + d, L > 0.f ? acc / L : 0.f);
+        const int64_t o = (static_cast<int64_t>(b) * p.num_heads + h) * D + 4 * d4;
+        store_out2(p, o, acc.x * inv, acc.y * inv);
+        store_out2(p, o + 2, acc.z * inv, acc.w * inv);
     }
     cluster_sync_all();   // peers have finished reading this CTA's shared memory
 }

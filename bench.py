@@ -72,6 +72,22 @@ def decode_alg_bytes(lens, hq, hkv, d, bs, elem) -> int:
     return kv_bytes(lens, hkv, d, elem) + B * hq * d * elem + B * hq * d * 4 + tbl + B * 4
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings over the process group (a
+    barrier-free all-reduce; the only cross-rank traffic of the benchmark)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(world: int, bytes_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own batch each step
+    (weak scaling), and a step lasts as long as the slowest rank's."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -439,15 +455,13 @@ def run_ours(args, rank, world, local_rank):
     ms_step = ms_total / steps_timed
     e2e_ms_step = e2e_s * 1e3 / e2e_steps
     if world > 1:
-        t = torch.tensor([ms_step, e2e_ms_step, decode_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_ms_step, decode_ms = (float(x) for x in t.tolist())
+        ms_step, e2e_ms_step, decode_ms = max_over_ranks([ms_step, e2e_ms_step, decode_ms], "cuda")
 
     lens0 = views[0]["lens_h"]
     step_kv = kv_bytes(lens0, hkv, d, elem)          # per batch; both batches have equal totals for qwen3/long
     avg_kv = np.mean([kv_bytes(v["lens_h"], hkv, d, elem) for v in views])
-    value = world * avg_kv / (ms_step * 1e-3) / 1e9
-    e2e_value = world * avg_kv / (e2e_ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, avg_kv, ms_step)
+    e2e_value = whole_job_gbs(world, avg_kv, e2e_ms_step)
     alg = np.mean([decode_alg_bytes(v["lens_h"], hq, hkv, d, bs, elem) for v in views])
     achieved = alg / (decode_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()

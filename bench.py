@@ -46,13 +46,32 @@ FALLBACK_HBM_GBS = 6800.0
 # ---------------------------------------------------------------------------
 # workload description
 # ---------------------------------------------------------------------------
-def build_workload(config: str, rank: int, copies: int):
+def build_workload(config: str, rank: int, copies: int, block_size: int = 16, layout: str = "paged"):
+    """The workload's batch (``copies`` disjoint batches) and its description.
+    ``layout`` "contiguous" gives the same lengths in a contiguous cache of
+    one maximum-length reservation per sequence (the unpaged baseline)."""
+    if layout == "contiguous":
+        nb = per_batch(config)
+        if config == "qwen3":
+            lens, hq, L = [workloads.QWEN3_TOKENS] * (nb * copies), 32, workloads.QWEN3_TOKENS
+        elif config == "long":
+            lens, hq, L = [workloads.LONG_TOKENS] * (nb * copies), 64, workloads.LONG_TOKENS
+        else:
+            lens, hq, L = workloads.gqa_lengths(nb * copies), 32, 4096
+        desc = "%s, contiguous cache: %d seqs x %d reserved rows (lengths as the paged workload), Hq %d, Hkv 8, D 128, bf16" % (
+            config, nb, L, hq)
+        return workloads.contiguous(config, lens, hq, 8, 128, L), desc
     if config == "qwen3":
-        return workloads.qwen3(num_seqs=16, copies=copies), "qwen3-8b layer: 16 seqs x 4164 tokens, Hq 32, Hkv 8, D 128, bf16, block 16, pool 38348 blocks"
+        return workloads.qwen3(num_seqs=16, copies=copies, block_size=block_size), \
+            "qwen3-8b layer: 16 seqs x 4164 tokens, Hq 32, Hkv 8, D 128, bf16, block %d, pool %d blocks" % (
+                block_size, workloads.QWEN3_POOL_BLOCKS * 16 // block_size)
     if config == "long":
-        return workloads.long_context(block_size=16, num_seqs=4, copies=copies), "long context: 4 seqs x 32768 tokens, Hq 64, Hkv 8, D 128, bf16, block 16"
+        return workloads.long_context(block_size=block_size, num_seqs=4, copies=copies), \
+            "long context: 4 seqs x 32768 tokens, Hq 64, Hkv 8, D 128, bf16, block %d" % block_size
     if config == "gqa":
-        return workloads.gqa(num_seqs=64 * copies, num_blocks=20000 * copies), "llama gqa: 64 seqs, len U[512,4096], Hq 32, Hkv 8, D 128, bf16, block 16"
+        return workloads.gqa(num_seqs=64 * copies, num_blocks=20000 * copies * 16 // block_size,
+                             block_size=block_size), \
+            "llama gqa: 64 seqs, len U[512,4096], Hq 32, Hkv 8, D 128, bf16, block %d" % block_size
     raise SystemExit(f"unknown config {config}")
 
 
@@ -66,9 +85,10 @@ def kv_bytes(lens, hkv, d, elem) -> int:
 
 def decode_alg_bytes(lens, hq, hkv, d, bs, elem) -> int:
     """Algorithmic bytes of one decode launch: K/V of valid tokens, the query,
-    the fp32 output, the block-table entries used and the lengths."""
+    the fp32 output, the block-table entries used (none for a contiguous
+    cache, ``bs`` None) and the lengths."""
     B = len(lens)
-    tbl = sum(workloads.cdiv(int(n), bs) for n in lens) * 4
+    tbl = 0 if bs is None else sum(workloads.cdiv(int(n), bs) for n in lens) * 4
     return kv_bytes(lens, hkv, d, elem) + B * hq * d * elem + B * hq * d * 4 + tbl + B * 4
 
 
@@ -227,7 +247,7 @@ def cpu_baseline(batch, nseq_batch, budget_s=10.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    batch, desc = build_workload(args.config, 0, 1)
+    batch, desc = build_workload(args.config, 0, 1, args.block_size)
     nb = per_batch(args.config)
     nthreads = os.cpu_count() or 1
     # size each step's sample (whole sequences) so the K + W steps fit ~120 s
@@ -274,39 +294,60 @@ def run_ours(args, rank, world, local_rank):
     pa.load_library()
 
     copies = 2
-    batch, desc = build_workload(args.config, rank, copies)
+    contig = args.layout == "contiguous"
+    batch, desc = build_workload(args.config, rank, copies, args.block_size, args.layout)
     nb = per_batch(args.config)
-    hq, hkv, d, bs = batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size
+    hq, hkv, d = batch.num_heads, batch.num_kv_heads, batch.head_dim
+    bs = None if contig else batch.block_size
     elem = batch.elem_bytes
+    headline = not contig and bs == 16
 
     def dev(a):
         if a.dtype == np.uint16:
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
         return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
-    k_cache, v_cache = dev(batch.k_cache), dev(batch.v_cache)
-    seq_all = np.arange(batch.num_seqs, dtype=np.int32)
-    slots_all = pa.pa_compute_slot_mapping(batch.block_tables, seq_all, batch.new_pos, bs)
+    if contig:
+        # [B, L, Hkv, D]; the scatter sees it as a pool of one-token blocks
+        L = batch.max_seq_len
+        k_full, v_full = dev(batch.k), dev(batch.v)
+        k_cache = k_full.view(batch.num_seqs * L, 1, hkv, d)
+        v_cache = v_full.view(batch.num_seqs * L, 1, hkv, d)
+        slots_all = np.arange(batch.num_seqs, dtype=np.int64) * L + batch.new_pos
+    else:
+        k_cache, v_cache = dev(batch.k_cache), dev(batch.v_cache)
+        seq_all = np.arange(batch.num_seqs, dtype=np.int32)
+        slots_all = pa.pa_compute_slot_mapping(batch.block_tables, seq_all, batch.new_pos, bs)
     views = []
     for c in range(copies):
         sl = slice(c * nb, (c + 1) * nb)
         lens = batch.context_lens[sl]
         views.append({
-            "query": dev(batch.query[sl]), "tables": dev(batch.block_tables[sl]),
+            "query": dev(batch.query[sl]),
+            "tables": None if contig else dev(batch.block_tables[sl]),
+            "k": k_full[sl] if contig else None, "v": v_full[sl] if contig else None,
             "lens": dev(lens), "key": dev(batch.new_key[sl]), "value": dev(batch.new_value[sl]),
             "slots": torch.from_numpy(slots_all[sl].copy()).cuda(),
             "max_len": int(lens.max()), "lens_h": lens,
             "out": torch.empty((nb, hq, d), dtype=torch.float32, device="cuda"),
         })
-    ws_bytes = max(pa.pa_decode_workspace_size(nb, hq, hkv, d, bs, v["max_len"]) for v in views)
+    ws_bytes = max(pa.pa_decode_workspace_size(nb, hq, hkv, d, 16 if contig else bs, v["max_len"])
+                   for v in views)
     workspace = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
 
     def scatter(v):
         pa.pa_reshape_and_cache(v["key"], v["value"], k_cache, v_cache, v["slots"])
 
+    def decode_into(out, v, query, lens, tables):
+        if contig:
+            pa.pa_decode_contiguous(out, query, v["k"], v["v"], lens, v["max_len"], batch.scale,
+                                    workspace=workspace)
+        else:
+            pa.pa_decode(out, query, k_cache, v_cache, tables, lens, v["max_len"], batch.scale,
+                         workspace=workspace)
+
     def decode(v):
-        pa.pa_decode(v["out"], v["query"], k_cache, v_cache, v["tables"], v["lens"], v["max_len"],
-                     batch.scale, workspace=workspace)
+        decode_into(v["out"], v, v["query"], v["lens"], v["tables"])
 
     def step(i):
         v = views[i % copies]
@@ -404,7 +445,7 @@ def run_ours(args, rank, world, local_rank):
         sl = slice(c * nb, (c + 1) * nb)
         h_in.append({
             "query": torch.from_numpy(batch.query[sl].view(np.int16).copy()).pin_memory(),
-            "tables": torch.from_numpy(batch.block_tables[sl].copy()).pin_memory(),
+            "tables": None if contig else torch.from_numpy(batch.block_tables[sl].copy()).pin_memory(),
             "lens": torch.from_numpy(batch.context_lens[sl].copy()).pin_memory(),
             "key": torch.from_numpy(batch.new_key[sl].view(np.int16).copy()).pin_memory(),
             "value": torch.from_numpy(batch.new_value[sl].view(np.int16).copy()).pin_memory(),
@@ -412,12 +453,12 @@ def run_ours(args, rank, world, local_rank):
             "out": torch.empty((nb, hq, d), dtype=torch.float32).pin_memory(),
         })
     h2d = sum(h_in[0][k].numel() * h_in[0][k].element_size()
-              for k in ("query", "tables", "lens", "key", "value", "slots"))
+              for k in ("query", "tables", "lens", "key", "value", "slots") if h_in[0][k] is not None)
     d2h = h_in[0]["out"].numel() * 4
     dq = torch.empty((nb, hq, d), dtype=torch.bfloat16, device="cuda")
     dk = torch.empty((nb, hkv, d), dtype=torch.bfloat16, device="cuda")
     dvv = torch.empty_like(dk)
-    dt = torch.empty_like(views[0]["tables"])
+    dt = None if contig else torch.empty_like(views[0]["tables"])
     dl = torch.empty_like(views[0]["lens"])
     ds = torch.empty_like(views[0]["slots"])
     dout = torch.empty((nb, hq, d), dtype=torch.float32, device="cuda")
@@ -428,11 +469,12 @@ def run_ours(args, rank, world, local_rank):
         dq.view(torch.int16).copy_(h["query"], non_blocking=True)
         dk.view(torch.int16).copy_(h["key"], non_blocking=True)
         dvv.view(torch.int16).copy_(h["value"], non_blocking=True)
-        dt.copy_(h["tables"], non_blocking=True)
+        if dt is not None:
+            dt.copy_(h["tables"], non_blocking=True)
         dl.copy_(h["lens"], non_blocking=True)
         ds.copy_(h["slots"], non_blocking=True)
         pa.pa_reshape_and_cache(dk, dvv, k_cache, v_cache, ds)
-        pa.pa_decode(dout, dq, k_cache, v_cache, dt, dl, v["max_len"], batch.scale, workspace=workspace)
+        decode_into(dout, v, dq, dl, dt)
         h["out"].copy_(dout, non_blocking=True)
         torch.cuda.current_stream().synchronize()   # the result is read on the host
         return float(h["out"][0, 0, 0])
@@ -465,29 +507,40 @@ def run_ours(args, rank, world, local_rank):
     alg = np.mean([decode_alg_bytes(v["lens_h"], hq, hkv, d, bs, elem) for v in views])
     achieved = alg / (decode_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    traffic = profiled_traffic(args.config)
+    traffic = profiled_traffic(args.config) if headline else None
+    if contig:
+        kernel = "decode_mma_kernel<128,16> (contiguous)"
+    elif bs in (8, 16, 32, 64, 128, 256):
+        kernel = "decode_mma_kernel<128,%d>" % min(bs, 16)
+    else:
+        kernel = "decode_simt_kernel"
+    decode_launches = 2 if ws_bytes > 0 else 1      # a wide split adds the merge kernel
     line = {
-        "metric": "paged decode attention KV GB/s (Qwen3-8B shape)",
+        "metric": ("decode attention KV GB/s, contiguous cache (unpaged baseline)" if contig
+                   else "paged decode attention KV GB/s (Qwen3-8B shape)"),
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps_timed, "warmup": W,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded N(0,1), bf16-rounded; block placement a seeded random permutation)",
+        "dtype": "bf16",
+        "data": ("synthetic (seeded N(0,1), bf16-rounded; one contiguous reservation per sequence)" if contig else
+                 "synthetic (seeded N(0,1), bf16-rounded; block placement a seeded random permutation)"),
         "config": {"workload": desc,
                    "graphs": "%d steps per CUDA graph, %d batches alternate" % (GRAPH_STEPS, copies),
                    "l2": "inputs larger than L2: 2 batches of %.0f MB alternate" % (step_kv / 1e6),
-                   "step": "reshape_and_cache(%d tokens) + pa_decode (fused split-K + LSE merge)" % nb},
+                   "step": "reshape_and_cache(%d tokens) + %s" % (
+                       nb, "pa_decode_contiguous" if contig else "pa_decode (fused split-K + LSE merge)")},
         "tokens_per_s": world * nb / (ms_step * 1e-3),
         "pct_of_8tbs": 100.0 * value / HBM_NOMINAL_GBS,
         "pct_of_measured_hbm": 100.0 * value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "decode_mma_kernel<128,%d>" % min(bs, 16), "peak_kind": peak_kind,
+                     "kernel": kernel, "peak_kind": peak_kind,
                      "decode_us": decode_ms * 1e3, "alg_bytes_per_launch": int(alg)},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms_step, "steps": e2e_steps},
-        "gpu_launches": 2 * steps_timed,
+        "gpu_launches": (1 + decode_launches) * steps_timed,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not contig:
         line["cpu_baseline"] = cpu_baseline(batch, nb, budget_s=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -503,6 +556,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=["qwen3", "long", "gqa"], default="qwen3")
+    ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
+                    help="contiguous: the same lengths in one reservation per sequence, no block table")
+    ap.add_argument("--block-size", type=int, default=16, choices=[4, 8, 16, 32, 64, 128],
+                    help="tokens per block of the paged cache (the pool keeps its token count)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-steps", type=int, default=0,

@@ -149,6 +149,37 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
                            size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Decode attention over a contiguous (unpaged) cache: the baseline that
+ * paging is measured against.
+ * [P5] "The problem: reserving the maximum" (one buffer per request, sized
+ * for its maximum length) and "What paging costs" (indirection: attention
+ * reads through the block table, 20-26 % slower than a contiguous kernel of
+ * the time); [P1] "Why the attention kernel works at all" (the lookup cost
+ * is amortised over a block, single-digit percent).
+ *
+ *   k, v         [num_seqs, max_seq_len, num_kv_heads, head_dim] bf16:
+ *                sequence b's token t at row b * max_seq_len + t. No block
+ *                table: the same kernel as pa_decode, with the block id
+ *                lookup replaced by the token offset.
+ *   max_seq_len  the reservation per sequence (rows per sequence).
+ *   context_lens [num_seqs] int32, each in [0, max_seq_len] (larger values
+ *                are clamped to max_seq_len).
+ *   max_context_len  host upper bound of context_lens, <= max_seq_len.
+ *   workspace    as pa_decode, sized by pa_decode_workspace_size() with
+ *                block_size 16.
+ *   Other arguments as pa_decode. Supported: bf16 query and cache (F32
+ *   returns PA_ERR_UNSUPPORTED), head_dim 64 or 128,
+ *   num_seqs * max_seq_len < 2^31.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_decode_contiguous(void *out, pa_dtype out_dtype, const void *query,
+                                      pa_dtype q_dtype, const void *k, const void *v,
+                                      pa_dtype kv_dtype, const int32_t *context_lens,
+                                      int num_seqs, int num_heads, int num_kv_heads,
+                                      int head_dim, int max_seq_len, int max_context_len,
+                                      float scale, void *workspace, size_t workspace_bytes,
+                                      void *stream);
+
+/* ------------------------------------------------------------------------
  * Decode for callers that cannot allocate device memory. (The source pages
  * have no counterpart: this is a library convenience.)
  *

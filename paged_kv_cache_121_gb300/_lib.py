@@ -35,6 +35,9 @@ SIGNATURES = {
     "pa_decode": (c_int, [c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p,
                           c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                           c_float, c_void_p, c_size_t, c_void_p]),
+    "pa_decode_contiguous": (c_int, [c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                     c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_float,
+                                     c_void_p, c_size_t, c_void_p]),
     "pa_decode_static_scratch": (c_int, [c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_int,
                                          c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                          c_int, c_int, c_int, c_float, c_void_p]),

@@ -105,6 +105,20 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, max_cont
                                 _stream(stream)), "pa_decode")
 
 
+def pa_decode_contiguous(out, query, k, v, context_lens, max_context_len, scale, workspace=None,
+                         stream=None) -> None:
+    """Decode attention over a contiguous cache ``k``, ``v`` [B, max_seq_len,
+    Hkv, D] (bfloat16, no block table): the unpaged baseline. ``workspace``
+    as for :func:`pa_decode`, sized with block_size 16."""
+    B, L, hkv, d = (int(x) for x in k.shape)
+    _, hq, _ = (int(x) for x in query.shape)
+    ws_bytes = int(workspace.numel() * workspace.element_size()) if workspace is not None else 0
+    _check(_lib.load().pa_decode_contiguous(_ptr(out), _dtype(out), _ptr(query), _dtype(query), _ptr(k),
+                                           _ptr(v), _dtype(k), _ptr(context_lens), B, hq, hkv, d, L,
+                                           int(max_context_len), float(scale), _ptr(workspace), ws_bytes,
+                                           _stream(stream)), "pa_decode_contiguous")
+
+
 def pa_decode_static_scratch(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len,
                              scale, stream=None) -> None:
     """pa_decode without a workspace argument: a context split is merged

@@ -27,6 +27,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kCtasPerSmMma = 2;      // resident CTAs per SM the split plan aims at
 constexpr int kCtasPerSmSimt = 2;     //   (tensor-core / CUDA-core kernel)
 constexpr int kMmaHeadsPerCta = 4;    // KV heads per tensor-core CTA (consumer warps)
+constexpr int kContiguousTile = 16;   // tokens per tile of a contiguous cache
 constexpr int kMmaRingKiB = 96;       // shared-memory ring per tensor-core CTA
 constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
 
@@ -108,7 +109,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 4-D view of a bf16 cache [num_blocks, block_size, Hkv, D] (innermost first:
 // D, Hkv, block_size, num_blocks); box = 64 dims x 1 head x box_tokens tokens
 // x 1 block, 128-byte swizzle. Out-of-range block ids read as zeros.
-pa_status make_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int block_size,
+pa_status make_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int64_t block_size,
                          int num_kv_heads, int head_dim, int box_tokens) {
     auto enc = tensor_map_encoder();
     if (!enc) return PA_ERR_CUDA;
@@ -256,10 +257,14 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
             const int need = decode_mma_cluster_bytes(s.head_dim, p.heads_per_cta);
             if (p.ring_bytes < need) p.ring_bytes = static_cast<int>(cdiv64(need, stage) * stage);
         }
+        // a contiguous cache [B, stride, Hkv, D] is mapped as one block of B * stride tokens
+        const bool contig = p.contig_stride > 0;
+        const int64_t map_blocks = contig ? 1 : s.num_blocks;
+        const int64_t map_tokens = contig ? static_cast<int64_t>(s.num_seqs) * p.contig_stride : s.block_size;
         CUtensorMap tk, tv;
-        pa_status st = make_cache_map(&tk, p.k_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim, tt);
+        pa_status st = make_cache_map(&tk, p.k_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, tt);
         if (st != PA_OK) return st;
-        st = make_cache_map(&tv, p.v_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim, tt);
+        st = make_cache_map(&tv, p.v_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, tt);
         if (st != PA_OK) return st;
         e = launch_decode_mma(p, tk, tv, grid, stream);
     } else {
@@ -287,6 +292,60 @@ void fill_common(DecodeParams &p, const DecodeShape &s, const void *query, pa_dt
     p.group = s.num_heads / s.num_kv_heads;
     p.q_bf16 = q_dtype == PA_BF16;
     p.scale_log2 = scale * kLog2e;
+}
+
+// Plan, check the pointers and launch one decode (paged when contig_stride
+// is 0, else over a contiguous cache [num_seqs, contig_stride, Hkv, D]).
+// The shape and dtypes have been checked by the caller.
+pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, const void *query,
+                         pa_dtype q_dtype, const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                         const int32_t *block_tables, const int32_t *context_lens, int contig_stride,
+                         float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!out || !query || !k_cache || !v_cache || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    int dev;
+    pa_status st = current_device(&dev);
+    if (st != PA_OK) return st;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PA_ERR_CUDA;
+
+    Plan pl = plan_split(s, sms, use_mma(s, kv_dtype == PA_BF16));
+    DecodeParams p;
+    fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
+    p.contig_stride = contig_stride;
+    p.out = out;
+    p.out_bf16 = out_dtype == PA_BF16;
+    p.ntile = pl.ntile;
+    p.heads_per_cta = pl.heads_per_cta;
+    if (workspace == nullptr && workspace_bytes == 0 && !pl.cluster) {
+        // no scratch: the tensor-core kernel keeps a split it can merge within
+        // a cluster; otherwise one CTA per (sequence, KV-head group, head tile)
+        const int64_t nblk = std::max<int64_t>(1, cdiv64(s.max_ctx, s.block_size));
+        if (pl.mma && pl.nsplit > 1) {
+            const int64_t pb = cdiv64(nblk, std::min(pl.nsplit, kMaxClusterSplits));
+            pl.part_blocks = static_cast<int>(pb);
+            pl.nsplit = static_cast<int>(cdiv64(nblk, pb));
+            pl.cluster = pl.nsplit > 1;
+        } else {
+            pl.part_blocks = static_cast<int>(nblk);
+            pl.nsplit = 1;
+        }
+    }
+    p.nsplit = pl.nsplit;
+    p.part_blocks = pl.part_blocks;
+    p.cluster_merge = pl.cluster ? 1 : 0;
+    if (pl.cluster) {
+        p.mode = kModeFused;
+    } else if (pl.nsplit > 1) {
+        const WorkspaceLayout wl = workspace_layout(s, pl);
+        if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+        return launch_split_and_merge(s, p, kv_dtype, dev, workspace, wl, out, out_dtype == PA_BF16,
+                                      as_stream(stream));
+    } else {
+        p.mode = kModeFinal;
+    }
+    return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
 }
 
 }  // namespace
@@ -417,50 +476,28 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
     if (!valid_dtype(out_dtype) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
     if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
     if (num_seqs == 0) return PA_OK;
-    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
-        return PA_ERR_INVALID_ARG;
-    int dev;
-    if ((st = current_device(&dev)) != PA_OK) return st;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return PA_ERR_CUDA;
+    if (!block_tables) return PA_ERR_INVALID_ARG;
+    return decode_planned(s, out, out_dtype, query, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                          context_lens, 0, scale, workspace, workspace_bytes, stream);
+}
 
-    Plan pl = plan_split(s, sms, use_mma(s, kv_dtype == PA_BF16));
-    DecodeParams p;
-    fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
-    p.out = out;
-    p.out_bf16 = out_dtype == PA_BF16;
-    p.ntile = pl.ntile;
-    p.heads_per_cta = pl.heads_per_cta;
-    if (workspace == nullptr && workspace_bytes == 0 && !pl.cluster) {
-        // no scratch: the tensor-core kernel keeps a split it can merge within
-        // a cluster; otherwise one CTA per (sequence, KV-head group, head tile)
-        const int64_t nblk = std::max<int64_t>(1, cdiv64(max_context_len, block_size));
-        if (pl.mma && pl.nsplit > 1) {
-            const int64_t pb = cdiv64(nblk, std::min(pl.nsplit, kMaxClusterSplits));
-            pl.part_blocks = static_cast<int>(pb);
-            pl.nsplit = static_cast<int>(cdiv64(nblk, pb));
-            pl.cluster = pl.nsplit > 1;
-        } else {
-            pl.part_blocks = static_cast<int>(nblk);
-            pl.nsplit = 1;
-        }
-    }
-    p.nsplit = pl.nsplit;
-    p.part_blocks = pl.part_blocks;
-    p.cluster_merge = pl.cluster ? 1 : 0;
-    if (pl.cluster) {
-        p.mode = kModeFused;
-    } else if (pl.nsplit > 1) {
-        const WorkspaceLayout wl = workspace_layout(s, pl);
-        if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-        return launch_split_and_merge(s, p, kv_dtype, dev, workspace, wl, out, out_dtype == PA_BF16,
-                                      as_stream(stream));
-    } else {
-        p.mode = kModeFinal;
-    }
-    return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
+PA_API pa_status pa_decode_contiguous(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
+                                      const void *k, const void *v, pa_dtype kv_dtype,
+                                      const int32_t *context_lens, int num_seqs, int num_heads,
+                                      int num_kv_heads, int head_dim, int max_seq_len, int max_context_len,
+                                      float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    if (max_seq_len <= 0 || max_context_len > max_seq_len) return PA_ERR_INVALID_ARG;
+    const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, kContiguousTile,
+                        static_cast<int>(cdiv64(max_seq_len, kContiguousTile)), 1, max_context_len};
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    if (!valid_dtype(out_dtype) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
+    if (kv_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(num_seqs) * max_seq_len > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    return decode_planned(s, out, out_dtype, query, q_dtype, k, v, kv_dtype, nullptr, context_lens,
+                          max_seq_len, scale, workspace, workspace_bytes, stream);
 }
 
 PA_API pa_status pa_decode_splitk(float *tmp_out, float *max_logits, float *exp_sums,

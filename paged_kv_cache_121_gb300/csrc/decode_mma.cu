@@ -370,7 +370,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     if (warp == hpc) {
         // ------------------------------ producer ------------------------------
-        const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks + w.blk_begin;
+        // paged: the tile's block id from the table; contiguous: token offset only
+        const bool contig = p.contig_stride > 0;
+        const int32_t *table =
+            contig ? nullptr : p.block_tables + static_cast<int64_t>(b) * p.max_blocks + w.blk_begin;
+        const int contig_tok0 = contig ? b * p.contig_stride + tok_begin : 0;
         uint64_t policy = 0;
         if (lane == 0) {
             tma_prefetch_desc(&tmap_k);
@@ -378,14 +382,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             policy = l2_policy_evict_first();
         }
         // entry for tile i = table[i / tiles_per_block], fetched 32 tiles at a time, one chunk ahead
-        int cur = lane < ntiles ? table[lane / tiles_per_block] : 0;
-        int nxt = 32 + lane < ntiles ? table[(32 + lane) / tiles_per_block] : 0;
+        int cur = !contig && lane < ntiles ? table[lane / tiles_per_block] : 0;
+        int nxt = !contig && 32 + lane < ntiles ? table[(32 + lane) / tiles_per_block] : 0;
         int issued = 0;
         const int head0 = hgrp * hpc;
         for (int i = 0; i < ntiles; ++i) {
             if ((i & 31) == 0 && i > 0) {
                 cur = nxt;
-                nxt = i + 32 + lane < ntiles ? table[(i + 32 + lane) / tiles_per_block] : 0;
+                nxt = !contig && i + 32 + lane < ntiles ? table[(i + 32 + lane) / tiles_per_block] : 0;
             }
             const int phys = __shfl_sync(0xffffffffu, cur, i & 31);
             int ok = 1;
@@ -404,7 +408,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const uint32_t full = smem_addr(&bars[s]);
                     mbar_arrive_expect_tx(full, static_cast<uint32_t>(stage_bytes));
                     const uint32_t kdst = smem_addr(smem + s * stage_bytes);
-                    const int tok0 = (i % tiles_per_block) * TT;
+                    const int tok0 = contig ? contig_tok0 + i * TT : (i % tiles_per_block) * TT;
                     for (int h = 0; h < hpc; ++h) {
 #pragma unroll
                         for (int hh = 0; hh < C::kHalves; ++hh) {

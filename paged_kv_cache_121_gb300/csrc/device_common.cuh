@@ -37,6 +37,8 @@ struct DecodeParams {
     int *status;         // device status word
     int num_seqs, num_heads, num_kv_heads, head_dim, block_size;
     int max_blocks, num_blocks;
+    int contig_stride;   // > 0: contiguous cache [num_seqs, contig_stride, Hkv, D] (no
+                         // block table; block_size is then the tile length)
     int group;           // num_heads / num_kv_heads
     int ntile;           // cdiv(group, 16)
     int heads_per_cta;   // KV heads one CTA serves (grid.y = Hkv / heads_per_cta * ntile)
@@ -248,7 +250,7 @@ __device__ __forceinline__ SeqWork seq_work(const DecodeParams &p, int b, int pa
     SeqWork w;
     int len = p.context_lens[b];
     if (len < 0) len = 0;
-    const int cap = p.max_blocks * p.block_size;
+    const int cap = p.contig_stride > 0 ? p.contig_stride : p.max_blocks * p.block_size;
     if (len > cap) len = cap;
     int nblk = (len + p.block_size - 1) / p.block_size;
     int nparts = (nblk + p.part_blocks - 1) / p.part_blocks;

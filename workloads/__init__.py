@@ -189,22 +189,24 @@ def gqa_lengths(num_seqs: int = 64, lo: int = 512, hi: int = 4096, seed: int = S
     return np.random.default_rng(seed).integers(lo, hi + 1, size=num_seqs).astype(np.int32)
 
 
-def gqa(num_seqs: int = 64, num_blocks: int = 20000) -> DecodeBatch:
+def gqa(num_seqs: int = 64, num_blocks: int = 20000, block_size: int = 16) -> DecodeBatch:
     """Llama-style GQA batch: lengths U[512, 4096], Hq 32, Hkv 8, D 128, blocks of 16."""
-    return make_batch("gqa", gqa_lengths(num_seqs), 32, 8, 128, 16, num_blocks, bf16=True)
+    return make_batch("gqa", gqa_lengths(num_seqs), 32, 8, 128, block_size, num_blocks, bf16=True)
 
 
 QWEN3_TOKENS = 4164          # 4,100-token prompt + 64 generated
 QWEN3_POOL_BLOCKS = 38348    # 613,568 cache tokens / 16
 
 
-def qwen3(num_seqs: int = 16, copies: int = 1) -> DecodeBatch:
+def qwen3(num_seqs: int = 16, copies: int = 1, block_size: int = 16) -> DecodeBatch:
     """Qwen3-8B-shaped layer: ``num_seqs * copies`` sequences of 4,164 tokens,
     Hq 32, Hkv 8, D 128, bf16, blocks of 16 scattered over a 38,348-block pool.
     ``copies`` > 1 draws several disjoint batches in one pool (consecutive
-    timed steps then read disjoint memory)."""
+    timed steps then read disjoint memory). Another ``block_size`` keeps the
+    pool at 613,568 tokens."""
     lens = np.full(num_seqs * copies, QWEN3_TOKENS, dtype=np.int32)
-    return make_batch("qwen3", lens, 32, 8, 128, 16, QWEN3_POOL_BLOCKS, bf16=True)
+    return make_batch("qwen3", lens, 32, 8, 128, block_size, QWEN3_POOL_BLOCKS * 16 // block_size,
+                      bf16=True)
 
 
 LONG_TOKENS = 32768
@@ -218,6 +220,78 @@ def long_context(block_size: int = 16, num_seqs: int = 4, copies: int = 1) -> De
     lens = np.full(num_seqs * copies, LONG_TOKENS, dtype=np.int32)
     return make_batch("long", lens, 64, 8, 128, block_size,
                       copies * LONG_POOL_TOKENS // block_size, bf16=True)
+
+
+@dataclasses.dataclass
+class ContiguousBatch:
+    """One decode step's inputs over a contiguous (unpaged) cache: each
+    sequence owns ``max_seq_len`` consecutive rows, as under a per-request
+    maximum-length reservation.
+
+      query        [B, Hq, D]              uint16 bf16 bits
+      k, v         [B, max_seq_len, Hkv, D] uint16 bf16 bits; rows at or past a
+                   sequence's length hold zeros, or NaN with ``tail_nan``
+      context_lens [B] int32
+      new_key, new_value [B, Hkv, D]; new_pos [B] (= context_len - 1)
+    """
+    name: str
+    query: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    context_lens: np.ndarray
+    new_key: np.ndarray
+    new_value: np.ndarray
+    new_pos: np.ndarray
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    scale: float
+    bf16: bool = True
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.k.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.context_lens.size else 0
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2
+
+
+BF16_NAN_BITS = 0x7FC0
+
+
+def contiguous(name: str, context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
+               max_seq_len: int, tail_nan: bool = False, seed_values: int = SEED_VALUES) -> ContiguousBatch:
+    """Draw a bf16 decode batch in the contiguous layout (N(0,1) rows for each
+    sequence's tokens, seeded like ``make_batch``)."""
+    lens = np.asarray(context_lens, dtype=np.int32)
+    B = lens.size
+    if B and int(lens.max()) > max_seq_len:
+        raise ValueError("a length exceeds max_seq_len")
+    rng = np.random.default_rng(seed_values)
+    shape = (B, max_seq_len, num_kv_heads, head_dim)
+    fill = np.uint16(BF16_NAN_BITS) if tail_nan else np.uint16(0)
+    k = np.full(shape, fill, dtype=np.uint16)
+    v = np.full(shape, fill, dtype=np.uint16)
+    for b in range(B):
+        n = int(lens[b])
+        k[b, :n] = _normal(rng, (n, num_kv_heads, head_dim), True)
+        v[b, :n] = _normal(rng, (n, num_kv_heads, head_dim), True)
+    query = _normal(rng, (B, num_heads, head_dim), True)
+    new_key = _normal(rng, (B, num_kv_heads, head_dim), True)
+    new_value = _normal(rng, (B, num_kv_heads, head_dim), True)
+    return ContiguousBatch(name=name, query=query, k=k, v=v, context_lens=lens, new_key=new_key,
+                           new_value=new_value, new_pos=np.maximum(lens - 1, 0).astype(np.int32),
+                           num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                           scale=1.0 / math.sqrt(head_dim))
 
 
 @dataclasses.dataclass

@@ -334,6 +334,8 @@ def run_ours(args, rank, world, local_rank):
     ws_bytes = max(pa.pa_decode_workspace_size(nb, hq, hkv, d, 16 if contig else bs, v["max_len"])
                    for v in views)
     workspace = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    plan = pa.pa_decode_plan(nb, hq, hkv, d, 16 if contig else bs, max(v["max_len"] for v in views),
+                             with_workspace=True)
 
     def scatter(v):
         pa.pa_reshape_and_cache(v["key"], v["value"], k_cache, v_cache, v["slots"])
@@ -514,7 +516,7 @@ def run_ours(args, rank, world, local_rank):
         kernel = "decode_mma_kernel<128,%d>" % min(bs, 16)
     else:
         kernel = "decode_simt_kernel"
-    decode_launches = 2 if ws_bytes > 0 else 1      # a wide split adds the merge kernel
+    decode_launches = plan["kernel_launches"]       # a wide split adds the merge kernel
     line = {
         "metric": ("decode attention KV GB/s, contiguous cache (unpaged baseline)" if contig
                    else "paged decode attention KV GB/s (Qwen3-8B shape)"),
@@ -526,6 +528,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": desc,
                    "graphs": "%d steps per CUDA graph, %d batches alternate" % (GRAPH_STEPS, copies),
                    "l2": "inputs larger than L2: 2 batches of %.0f MB alternate" % (step_kv / 1e6),
+                   "plan": plan,
                    "step": "reshape_and_cache(%d tokens) + %s" % (
                        nb, "pa_decode_contiguous" if contig else "pa_decode (fused split-K + LSE merge)")},
         "tokens_per_s": world * nb / (ms_step * 1e-3),

@@ -140,6 +140,24 @@ PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *blo
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                        int head_dim, int block_size, int max_context_len);
 
+/* How pa_decode will run a problem on the current device (host only, no
+ * launch): which kernel, how the context is split and merged, and how many
+ * kernels one call launches. with_workspace: 1 if the call will pass a
+ * workspace of pa_decode_workspace_size() bytes, 0 if it passes none. */
+typedef struct pa_decode_plan_t {
+    int tensor_cores;       /* 1: tensor-core kernel; 0: CUDA-core kernel */
+    int heads_per_cta;      /* KV heads one CTA serves */
+    int num_splits;         /* partitions per context (1: not split) */
+    int partition_tokens;   /* tokens per partition */
+    int cluster_merge;      /* 1: partitions merged inside a thread-block cluster */
+    int kernel_launches;    /* kernels one call launches: 1, or 2 (decode + merge) */
+    size_t workspace_bytes; /* workspace the plan uses (0: none) */
+} pa_decode_plan_t;
+
+PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_context_len, pa_dtype kv_dtype,
+                                int with_workspace, pa_decode_plan_t *plan);
+
 PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
                            const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
                            const int32_t *block_tables, const int32_t *context_lens,

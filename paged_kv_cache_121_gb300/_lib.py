@@ -32,6 +32,7 @@ SIGNATURES = {
     "pa_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                c_int, c_void_p]),
     "pa_decode_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
+    "pa_decode_plan": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "pa_decode": (c_int, [c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p,
                           c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                           c_float, c_void_p, c_size_t, c_void_p]),

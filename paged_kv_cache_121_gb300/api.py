@@ -89,6 +89,27 @@ def pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_
                                                     block_size, max_context_len))
 
 
+class DecodePlan(ctypes.Structure):
+    """pa_decode_plan_t: how pa_decode runs a problem on the current device."""
+    _fields_ = [("tensor_cores", ctypes.c_int), ("heads_per_cta", ctypes.c_int),
+                ("num_splits", ctypes.c_int), ("partition_tokens", ctypes.c_int),
+                ("cluster_merge", ctypes.c_int), ("kernel_launches", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self) -> dict:
+        return {name: int(getattr(self, name)) for name, _ in self._fields_}
+
+
+def pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                   kv_dtype=PA_BF16, with_workspace=True) -> dict:
+    """The plan pa_decode uses for this problem (host only; no launch)."""
+    plan = DecodePlan()
+    _check(_lib.load().pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                     max_context_len, int(kv_dtype), int(bool(with_workspace)),
+                                     ctypes.byref(plan)), "pa_decode_plan")
+    return plan.as_dict()
+
+
 def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
               workspace=None, stream=None) -> None:
     """Paged decode attention into ``out`` [B, Hq, D] (float32 or bfloat16).

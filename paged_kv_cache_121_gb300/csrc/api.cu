@@ -145,18 +145,23 @@ pa_status check_shape(const DecodeShape &s) {
 }
 
 struct Plan {
-    bool mma;
+    bool mma;           // tensor-core kernel (else CUDA-core)
     bool cluster;       // split merged through distributed shared memory (no workspace)
     int heads_per_cta;
     int ntile;
     int nsplit;
-    int part_blocks;
+    int part_tokens;    // tokens per partition
 };
 
 bool use_mma(const DecodeShape &s, bool bf16) { return bf16 && decode_mma_supported(s.head_dim, s.block_size); }
 
+// Partition granularity: the tensor-core kernel's tile, the CUDA-core
+// kernel's block.
+int split_granule(const DecodeShape &s, bool mma) { return mma ? decode_mma_tile_tokens(s.block_size) : s.block_size; }
+
 // Split each (sequence, KV-head group, head tile) context so that about
 // sm_count * ctas_per_sm CTAs exist, with at least kMinSplitTokens per piece.
+// Partitions are whole granules, sized evenly over max_context_len.
 Plan plan_split(const DecodeShape &s, int sms, bool mma) {
     Plan pl;
     pl.mma = mma;
@@ -165,14 +170,15 @@ Plan plan_split(const DecodeShape &s, int sms, bool mma) {
     pl.ntile = (group + kRowsPerTile - 1) / kRowsPerTile;
     const int64_t units =
         static_cast<int64_t>(s.num_seqs) * (s.num_kv_heads / pl.heads_per_cta) * pl.ntile;
-    const int64_t nblk = std::max<int64_t>(1, cdiv64(s.max_ctx, s.block_size));
+    const int gran = split_granule(s, mma);
+    const int64_t ngran = std::max<int64_t>(1, cdiv64(s.max_ctx, gran));
     const int per_sm = ctas_per_sm_override() ? ctas_per_sm_override() : (mma ? kCtasPerSmMma : kCtasPerSmSimt);
     const int64_t cap = static_cast<int64_t>(sms) * per_sm;
     int64_t nsplit = 1;
     if (units > 0 && units < cap) {
         nsplit = cap / units;
-        const int64_t min_pb = std::max<int64_t>(1, cdiv64(kMinSplitTokens, s.block_size));
-        nsplit = std::min(nsplit, std::max<int64_t>(1, nblk / min_pb));
+        const int64_t min_pg = std::max<int64_t>(1, cdiv64(kMinSplitTokens, gran));
+        nsplit = std::min(nsplit, std::max<int64_t>(1, ngran / min_pg));
         nsplit = std::min<int64_t>(nsplit, kMaxSplits);
     }
     // Tensor-core kernel: merge inside a cluster when the split fits one
@@ -183,13 +189,33 @@ Plan plan_split(const DecodeShape &s, int sms, bool mma) {
             nsplit = kMaxClusterSplits;
         pl.cluster = nsplit <= kMaxClusterSplits;
     }
-    const int64_t pb = cdiv64(nblk, nsplit);
-    pl.part_blocks = static_cast<int>(pb);
-    pl.nsplit = static_cast<int>(cdiv64(nblk, pb));
+    const int64_t pg = cdiv64(ngran, nsplit);
+    pl.part_tokens = static_cast<int>(pg * gran);
+    pl.nsplit = static_cast<int>(cdiv64(ngran, pg));
     if (pl.nsplit < 2) pl.cluster = false;
     if (pl.cluster) {
         // the cluster must span exactly the partitions of one context
         pl.nsplit = static_cast<int>(nsplit);
+    }
+    return pl;
+}
+
+// The plan pa_decode uses: with no workspace, a split the tensor-core kernel
+// cannot keep inside a cluster is trimmed to one (CUDA-core: not split).
+Plan plan_decode(const DecodeShape &s, int sms, bool mma, bool have_workspace) {
+    Plan pl = plan_split(s, sms, mma);
+    if (!have_workspace && !pl.cluster) {
+        const int gran = split_granule(s, mma);
+        const int64_t ngran = std::max<int64_t>(1, cdiv64(s.max_ctx, gran));
+        if (pl.mma && pl.nsplit > 1) {
+            const int64_t pg = cdiv64(ngran, std::min(pl.nsplit, kMaxClusterSplits));
+            pl.part_tokens = static_cast<int>(pg * gran);
+            pl.nsplit = static_cast<int>(cdiv64(ngran, pg));
+            pl.cluster = pl.nsplit > 1;
+        } else {
+            pl.part_tokens = static_cast<int>(ngran * gran);
+            pl.nsplit = 1;
+        }
     }
     return pl;
 }
@@ -211,13 +237,13 @@ WorkspaceLayout workspace_layout(const DecodeShape &s, const Plan &pl) {
     return w;
 }
 
-pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, int dev,
+pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, bool mma, int dev,
                         cudaStream_t stream);
 
 // Decode of a wide split: partitions in split-K form into the workspace, then
 // the merge kernel on the same stream.
-pa_status launch_split_and_merge(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, int dev,
-                                 void *workspace, const WorkspaceLayout &wl, void *out, bool out_bf16,
+pa_status launch_split_and_merge(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, bool mma,
+                                 int dev, void *workspace, const WorkspaceLayout &wl, void *out, bool out_bf16,
                                  cudaStream_t stream) {
     char *ws = static_cast<char *>(workspace);
     p.tmp_out = reinterpret_cast<float *>(ws + wl.o_off);
@@ -225,11 +251,11 @@ pa_status launch_split_and_merge(const DecodeShape &s, DecodeParams &p, pa_dtype
     p.exp_sums = reinterpret_cast<float *>(ws + wl.count_off);
     p.mode = kModeSplitK;
     p.cluster_merge = 0;
-    pa_status st = launch_decode(s, p, kv_dtype, dev, stream);
+    pa_status st = launch_decode(s, p, kv_dtype, mma, dev, stream);
     if (st != PA_OK) return st;
     const cudaError_t e = launch_lse_merge(out, out_bf16 ? 1 : 0, p.tmp_out, p.max_logits, p.exp_sums,
                                            p.context_lens, s.num_seqs, s.num_heads, s.head_dim,
-                                           p.nsplit, p.part_blocks * s.block_size, stream);
+                                           p.nsplit, p.part_tokens, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -239,8 +265,9 @@ pa_status check_dtypes(pa_dtype q_dtype, pa_dtype kv_dtype) {
     return PA_OK;
 }
 
-// Shared by pa_decode and pa_decode_splitk.
-pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, int dev,
+// Shared by pa_decode and pa_decode_splitk; `mma` picks the tensor-core
+// kernel (bf16, a supported block size, partitions of whole 16-token tiles).
+pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, bool mma, int dev,
                         cudaStream_t stream) {
     const bool bf16 = kv_dtype == PA_BF16;
     p.status = status_word(dev);
@@ -249,8 +276,8 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
                     static_cast<unsigned>((s.num_kv_heads / p.heads_per_cta) * p.ntile),
                     static_cast<unsigned>(s.num_seqs));
     cudaError_t e;
-    if (use_mma(s, bf16)) {
-        const int tt = decode_mma_tile_tokens(s.block_size);
+    if (mma) {
+        const int box = decode_mma_box_tokens(s.block_size);
         const int stage = decode_mma_stage_bytes(s.head_dim, s.block_size, p.heads_per_cta);
         p.ring_bytes = std::max(stage, (ring_kb() * 1024) / stage * stage);
         if (p.cluster_merge) {
@@ -262,9 +289,9 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
         const int64_t map_blocks = contig ? 1 : s.num_blocks;
         const int64_t map_tokens = contig ? static_cast<int64_t>(s.num_seqs) * p.contig_stride : s.block_size;
         CUtensorMap tk, tv;
-        pa_status st = make_cache_map(&tk, p.k_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, tt);
+        pa_status st = make_cache_map(&tk, p.k_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box);
         if (st != PA_OK) return st;
-        st = make_cache_map(&tv, p.v_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, tt);
+        st = make_cache_map(&tv, p.v_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box);
         if (st != PA_OK) return st;
         e = launch_decode_mma(p, tk, tv, grid, stream);
     } else {
@@ -310,7 +337,8 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
     const int sms = sm_count(dev);
     if (sms <= 0) return PA_ERR_CUDA;
 
-    Plan pl = plan_split(s, sms, use_mma(s, kv_dtype == PA_BF16));
+    const Plan pl = plan_decode(s, sms, use_mma(s, kv_dtype == PA_BF16),
+                                workspace != nullptr || workspace_bytes != 0);
     DecodeParams p;
     fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
     p.contig_stride = contig_stride;
@@ -318,34 +346,20 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
     p.out_bf16 = out_dtype == PA_BF16;
     p.ntile = pl.ntile;
     p.heads_per_cta = pl.heads_per_cta;
-    if (workspace == nullptr && workspace_bytes == 0 && !pl.cluster) {
-        // no scratch: the tensor-core kernel keeps a split it can merge within
-        // a cluster; otherwise one CTA per (sequence, KV-head group, head tile)
-        const int64_t nblk = std::max<int64_t>(1, cdiv64(s.max_ctx, s.block_size));
-        if (pl.mma && pl.nsplit > 1) {
-            const int64_t pb = cdiv64(nblk, std::min(pl.nsplit, kMaxClusterSplits));
-            pl.part_blocks = static_cast<int>(pb);
-            pl.nsplit = static_cast<int>(cdiv64(nblk, pb));
-            pl.cluster = pl.nsplit > 1;
-        } else {
-            pl.part_blocks = static_cast<int>(nblk);
-            pl.nsplit = 1;
-        }
-    }
     p.nsplit = pl.nsplit;
-    p.part_blocks = pl.part_blocks;
+    p.part_tokens = pl.part_tokens;
     p.cluster_merge = pl.cluster ? 1 : 0;
     if (pl.cluster) {
         p.mode = kModeFused;
     } else if (pl.nsplit > 1) {
         const WorkspaceLayout wl = workspace_layout(s, pl);
         if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-        return launch_split_and_merge(s, p, kv_dtype, dev, workspace, wl, out, out_dtype == PA_BF16,
+        return launch_split_and_merge(s, p, kv_dtype, pl.mma, dev, workspace, wl, out, out_dtype == PA_BF16,
                                       as_stream(stream));
     } else {
         p.mode = kModeFinal;
     }
-    return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
+    return launch_decode(s, p, kv_dtype, pl.mma, dev, as_stream(stream));
 }
 
 }  // namespace
@@ -381,13 +395,13 @@ int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes
     p.ntile = pl.ntile;
     p.heads_per_cta = pl.heads_per_cta;
     p.nsplit = pl.nsplit;
-    p.part_blocks = pl.part_blocks;
+    p.part_tokens = pl.part_tokens;
     p.cluster_merge = 0;
     if (pl.nsplit > 1)
-        return launch_split_and_merge(s, p, kv_dtype, dev, scratch, wl, c.out, out_dtype == PA_BF16,
+        return launch_split_and_merge(s, p, kv_dtype, pl.mma, dev, scratch, wl, c.out, out_dtype == PA_BF16,
                                       as_stream(stream));
     p.mode = kModeFinal;
-    return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
+    return launch_decode(s, p, kv_dtype, pl.mma, dev, as_stream(stream));
 }
 
 }  // namespace pa
@@ -463,6 +477,31 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_h
                     workspace_layout(s, plan_split(s, sms, false)).total);
 }
 
+PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_context_len, pa_dtype kv_dtype,
+                                int with_workspace, pa_decode_plan_t *plan) {
+    if (!plan || !valid_dtype(kv_dtype)) return PA_ERR_INVALID_ARG;
+    const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        std::max(1, block_size > 0 ? (max_context_len + block_size - 1) / block_size : 1),
+                        1, max_context_len};
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    int dev;
+    if ((st = current_device(&dev)) != PA_OK) return st;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PA_ERR_CUDA;
+    const Plan pl = plan_decode(s, sms, use_mma(s, kv_dtype == PA_BF16), with_workspace != 0);
+    const bool wide = !pl.cluster && pl.nsplit > 1;
+    plan->tensor_cores = pl.mma ? 1 : 0;
+    plan->heads_per_cta = pl.heads_per_cta;
+    plan->num_splits = pl.nsplit;
+    plan->partition_tokens = pl.part_tokens;
+    plan->cluster_merge = pl.cluster ? 1 : 0;
+    plan->kernel_launches = num_seqs == 0 ? 0 : (wide ? 2 : 1);
+    plan->workspace_bytes = wide ? workspace_layout(s, pl).total : 0;
+    return PA_OK;
+}
+
 PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
                            const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
                            const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
@@ -528,12 +567,15 @@ PA_API pa_status pa_decode_splitk(float *tmp_out, float *max_logits, float *exp_
     p.tmp_out = tmp_out;
     p.max_logits = max_logits;
     p.exp_sums = exp_sums;
+    // the tensor-core kernel cuts partitions at whole 16-token tiles
+    const bool mma = use_mma(s, kv_dtype == PA_BF16) &&
+                     partition_size % decode_mma_tile_tokens(block_size) == 0;
     p.ntile = (s.num_heads / s.num_kv_heads + kRowsPerTile - 1) / kRowsPerTile;
-    p.heads_per_cta = use_mma(s, kv_dtype == PA_BF16) ? decode_mma_heads_per_cta(s.num_kv_heads, heads_cap()) : 1;
+    p.heads_per_cta = mma ? decode_mma_heads_per_cta(s.num_kv_heads, heads_cap()) : 1;
     p.nsplit = static_cast<int>(P);
-    p.part_blocks = partition_size / block_size;
+    p.part_tokens = partition_size;
     p.mode = kModeSplitK;
-    return launch_decode(s, p, kv_dtype, dev, as_stream(stream));
+    return launch_decode(s, p, kv_dtype, mma, dev, as_stream(stream));
 }
 
 PA_API pa_status pa_lse_merge(void *out, pa_dtype out_dtype, const float *tmp_out,

@@ -7,11 +7,12 @@
 // head h reads KV head h / (Hq / Hkv).
 //
 // How. One CTA = one sequence x a group of up to 8 KV heads x up to 16 query
-// heads per KV head x one partition of the sequence's blocks.
-//  * The last warp walks the block table (read 32 entries at a time, a chunk
-//    ahead) and, per tile of 16 tokens (8 when blocks are 8 tokens), issues
-//    TMA tiled loads (cp.async.bulk.tensor) of the tile's K and V rows for
-//    every KV head of the group into one stage of a shared-memory ring;
+// heads per KV head x one partition of the sequence's tokens (whole tiles of
+// 16 tokens; a block of 32 or more tokens may straddle two partitions).
+//  * The last warp walks the block table (read 32 tiles' entries at a time, a
+//    chunk ahead) and, per 16-token tile (two blocks when blocks are 8 tokens),
+//    issues TMA tiled loads (cp.async.bulk.tensor) of the tile's K and V rows
+//    for every KV head of the group into one stage of a shared-memory ring;
 //    completion is counted on the stage's mbarrier. All heads of a block are
 //    requested back to back, so each block's K (and V) -- contiguous in the
 //    [num_blocks, block_size, Hkv, D] layout -- is fetched as one burst.
@@ -51,7 +52,7 @@ struct MmaCfg {
     static constexpr size_t kBarrierBytes = 2 * kMaxStages * sizeof(uint64_t);
     static size_t smem_bytes(int ring) { return 1024 + static_cast<size_t>(ring) + kBarrierBytes; }
     static_assert(kHalfBytes % 1024 == 0, "swizzled halves must stay 1024-byte aligned");
-    static_assert(TT == 8 || TT == 16, "tiles are 8 or 16 tokens");
+    static_assert(TT == 16, "tiles are 16 tokens (two 8-token blocks, or part of a larger block)");
 };
 
 constexpr float kRescaleSlack = 8.f;   // base-2 headroom before the running max is moved
@@ -310,7 +311,7 @@ __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, co
     cluster_sync_all();   // peers have finished reading this CTA's shared memory
 }
 
-template <int D, int TT, bool kCluster>
+template <int D, int TT, bool kCluster, bool kPairs>
 __global__ void __launch_bounds__(MmaCfg<D, TT>::kThreads, 1)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
@@ -334,7 +335,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // (one instantiation per epilogue keeps the other's registers out of the loop)
     constexpr bool cluster = kCluster;
-    if (w.blk_begin >= w.blk_end && !cluster) {
+    if (w.tok_begin >= w.tok_end && !cluster) {
         if (warp < hpc) {
             const int gh = hgrp * hpc + warp;
             warp_write_empty<D>(p, b, gh * p.group + tile * kRowsPerTile, part, rows, w.nparts, lane);
@@ -342,10 +343,16 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         return;
     }
     // (in a cluster every CTA takes part in the exchange, an empty partition included)
-    const int tok_begin = w.blk_begin * p.block_size;
-    const int tok_end = min(w.len, w.blk_end * p.block_size);
+    const int tok_begin = w.tok_begin;     // a multiple of TT (partitions are whole tiles)
+    const int tok_end = w.tok_end;
     const int ntiles = tok_end > tok_begin ? (tok_end - tok_begin + TT - 1) / TT : 0;
-    const int tiles_per_block = p.block_size / TT;
+    const int bs = p.block_size;
+    // A tile is TT tokens of one block, or (kPairs: blocks of TT / 2 tokens)
+    // two whole blocks back to back, one TMA box of box_rows rows each. (A
+    // separate instantiation: the second box's loads, even never taken,
+    // slow the single-box loop.)
+    constexpr int bpt = kPairs ? 2 : 1;
+    constexpr int box_rows = TT / bpt;
     const int stage_bytes = 2 * hpc * C::kHeadBytes;
     int nstages = p.ring_bytes / stage_bytes;
     if (nstages > C::kMaxStages) nstages = C::kMaxStages;
@@ -370,10 +377,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     if (warp == hpc) {
         // ------------------------------ producer ------------------------------
-        // paged: the tile's block id from the table; contiguous: token offset only
+        // paged: each box's block id from the table; contiguous: token offset only
         const bool contig = p.contig_stride > 0;
-        const int32_t *table =
-            contig ? nullptr : p.block_tables + static_cast<int64_t>(b) * p.max_blocks + w.blk_begin;
+        const int32_t *table = contig ? nullptr : p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
         const int contig_tok0 = contig ? b * p.contig_stride + tok_begin : 0;
         uint64_t policy = 0;
         if (lane == 0) {
@@ -381,17 +387,26 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tma_prefetch_desc(&tmap_v);
             policy = l2_policy_evict_first();
         }
-        // entry for tile i = table[i / tiles_per_block], fetched 32 tiles at a time, one chunk ahead
-        int cur = !contig && lane < ntiles ? table[lane / tiles_per_block] : 0;
-        int nxt = !contig && 32 + lane < ntiles ? table[(32 + lane) / tiles_per_block] : 0;
+        // Block id of box j of tile t; entries for 32 tiles are fetched at a
+        // time, one chunk ahead. Boxes past the context are not read (the
+        // table holds no entry for them).
+        auto entry = [&](int t, int j) -> int {
+            const int tok = tok_begin + t * TT + j * box_rows;
+            return (!contig && t < ntiles && tok < tok_end) ? table[tok / bs] : 0;
+        };
+        int cur0 = entry(lane, 0), cur1 = kPairs ? entry(lane, 1) : 0;
+        int nxt0 = entry(32 + lane, 0), nxt1 = kPairs ? entry(32 + lane, 1) : 0;
         int issued = 0;
         const int head0 = hgrp * hpc;
         for (int i = 0; i < ntiles; ++i) {
             if ((i & 31) == 0 && i > 0) {
-                cur = nxt;
-                nxt = !contig && i + 32 + lane < ntiles ? table[(i + 32 + lane) / tiles_per_block] : 0;
+                cur0 = nxt0;
+                cur1 = nxt1;
+                nxt0 = entry(i + 32 + lane, 0);
+                if (kPairs) nxt1 = entry(i + 32 + lane, 1);
             }
-            const int phys = __shfl_sync(0xffffffffu, cur, i & 31);
+            const int phys0 = __shfl_sync(0xffffffffu, cur0, i & 31);
+            const int phys1 = kPairs ? __shfl_sync(0xffffffffu, cur1, i & 31) : 0;
             int ok = 1;
             if (lane == 0) {
                 const int s = i % nstages, k = i / nstages;
@@ -405,16 +420,26 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     }
                 }
                 if (ok) {
+                    const int t0 = tok_begin + i * TT;
+                    // boxes with tokens in them (the last tile may hold fewer blocks)
+                    const int nbox = kPairs && t0 + box_rows < tok_end ? 2 : 1;
                     const uint32_t full = smem_addr(&bars[s]);
-                    mbar_arrive_expect_tx(full, static_cast<uint32_t>(stage_bytes));
+                    mbar_arrive_expect_tx(full, static_cast<uint32_t>(stage_bytes / bpt * nbox));
                     const uint32_t kdst = smem_addr(smem + s * stage_bytes);
-                    const int tok0 = contig ? contig_tok0 + i * TT : (i % tiles_per_block) * TT;
+                    const int tok0 = contig ? contig_tok0 + i * TT : t0 % bs;
+                    const int blk0 = contig ? 0 : phys0;
                     for (int h = 0; h < hpc; ++h) {
 #pragma unroll
                         for (int hh = 0; hh < C::kHalves; ++hh) {
                             const uint32_t off = h * C::kHeadBytes + hh * C::kHalfBytes;
-                            tma_load_4d(kdst + off, &tmap_k, hh * 64, head0 + h, tok0, phys, full, policy);
-                            tma_load_4d(kdst + v_off + off, &tmap_v, hh * 64, head0 + h, tok0, phys, full, policy);
+                            tma_load_4d(kdst + off, &tmap_k, hh * 64, head0 + h, tok0, blk0, full, policy);
+                            tma_load_4d(kdst + v_off + off, &tmap_v, hh * 64, head0 + h, tok0, blk0, full, policy);
+                            if (kPairs && nbox > 1) {
+                                const uint32_t off1 = off + box_rows * 128;
+                                tma_load_4d(kdst + off1, &tmap_k, hh * 64, head0 + h, 0, phys1, full, policy);
+                                tma_load_4d(kdst + v_off + off1, &tmap_v, hh * 64, head0 + h, 0, phys1, full,
+                                            policy);
+                            }
                         }
                     }
                     issued = i + 1;
@@ -541,39 +566,19 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
 
             // ---- O += P V ----
-            if constexpr (TT == 16) {
 #pragma unroll
-                for (int dn = 0; dn < D / 8; dn += 2) {
-                    const int mi = lane >> 3;
-                    const int tok = (mi & 1) * 8 + (lane & 7);
-                    const int c = dn + (mi >> 1);
-                    const uint32_t addr = vbase + (c >> 3) * C::kHalfBytes + tok * 128 +
-                                          (((c & 7) ^ (tok & 7)) << 4);
-                    uint32_t v0, v1, v2, v3;
-                    ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-                    mma_bf16_16816(st.o[dn], phi, v0, v1);
-                    mma_bf16_16816(st.o[dn + 1], phi, v2, v3);
-                    mma_bf16_16816(st.o[dn], plo, v0, v1);
-                    mma_bf16_16816(st.o[dn + 1], plo, v2, v3);
-                }
-            } else {
-#pragma unroll
-                for (int dn = 0; dn < D / 8; dn += 4) {
-                    const int tok = lane & 7;
-                    const int c = dn + (lane >> 3);
-                    const uint32_t addr = vbase + (c >> 3) * C::kHalfBytes + tok * 128 +
-                                          (((c & 7) ^ (tok & 7)) << 4);
-                    uint32_t v0, v1, v2, v3;
-                    ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-                    mma_bf16_16816(st.o[dn], phi, v0, 0u);
-                    mma_bf16_16816(st.o[dn + 1], phi, v1, 0u);
-                    mma_bf16_16816(st.o[dn + 2], phi, v2, 0u);
-                    mma_bf16_16816(st.o[dn + 3], phi, v3, 0u);
-                    mma_bf16_16816(st.o[dn], plo, v0, 0u);
-                    mma_bf16_16816(st.o[dn + 1], plo, v1, 0u);
-                    mma_bf16_16816(st.o[dn + 2], plo, v2, 0u);
-                    mma_bf16_16816(st.o[dn + 3], plo, v3, 0u);
-                }
+            for (int dn = 0; dn < D / 8; dn += 2) {
+                const int mi = lane >> 3;
+                const int tok = (mi & 1) * 8 + (lane & 7);
+                const int c = dn + (mi >> 1);
+                const uint32_t addr = vbase + (c >> 3) * C::kHalfBytes + tok * 128 +
+                                      (((c & 7) ^ (tok & 7)) << 4);
+                uint32_t v0, v1, v2, v3;
+                ldmatrix_x4_trans(addr, v0, v1, v2, v3);
+                mma_bf16_16816(st.o[dn], phi, v0, v1);
+                mma_bf16_16816(st.o[dn + 1], phi, v2, v3);
+                mma_bf16_16816(st.o[dn], plo, v0, v1);
+                mma_bf16_16816(st.o[dn + 1], plo, v2, v3);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[C::kMaxStages + s]));
@@ -602,20 +607,20 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
-template <int D, int TT>
+template <int D, int TT, bool kPairs>
 static cudaError_t launch_impl(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                dim3 grid, cudaStream_t stream) {
     using C = MmaCfg<D, TT>;
     const size_t smem = C::smem_bytes(p.ring_bytes);
     if (!p.cluster_merge) {
-        auto kern = decode_mma_kernel<D, TT, false>;
+        auto kern = decode_mma_kernel<D, TT, false, kPairs>;
         static unsigned long long done = 0;
         cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
         if (e != cudaSuccess) return e;
         kern<<<grid, 32 * (p.heads_per_cta + 1), smem, stream>>>(tk, tv, p);
         return cudaGetLastError();
     }
-    auto kern = decode_mma_kernel<D, TT, true>;
+    auto kern = decode_mma_kernel<D, TT, true, kPairs>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
     if (e != cudaSuccess) return e;
@@ -640,7 +645,9 @@ bool decode_mma_supported(int head_dim, int block_size) {
             block_size == 128 || block_size == 256);
 }
 
-int decode_mma_tile_tokens(int block_size) { return block_size < 16 ? block_size : 16; }
+int decode_mma_tile_tokens(int) { return 16; }
+
+int decode_mma_box_tokens(int block_size) { return block_size < 16 ? block_size : 16; }
 
 int decode_mma_heads_per_cta(int num_kv_heads, int max_heads) {
     for (int h = max_heads < MmaCfg<128, 16>::kMaxHeads ? max_heads : MmaCfg<128, 16>::kMaxHeads; h > 1; --h)
@@ -658,14 +665,13 @@ int decode_mma_cluster_bytes(int head_dim, int heads_per_cta) {
 
 cudaError_t launch_decode_mma(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                               dim3 grid, cudaStream_t stream) {
-    const int tt = decode_mma_tile_tokens(p.block_size);
-    if (p.head_dim == 128) {
-        if (tt == 16) return launch_impl<128, 16>(p, tk, tv, grid, stream);
-        if (tt == 8) return launch_impl<128, 8>(p, tk, tv, grid, stream);
-    } else if (p.head_dim == 64) {
-        if (tt == 16) return launch_impl<64, 16>(p, tk, tv, grid, stream);
-        if (tt == 8) return launch_impl<64, 8>(p, tk, tv, grid, stream);
-    }
+    const bool pairs = p.block_size < 16;     // blocks of 8: two per 16-token tile
+    if (p.head_dim == 128)
+        return pairs ? launch_impl<128, 16, true>(p, tk, tv, grid, stream)
+                     : launch_impl<128, 16, false>(p, tk, tv, grid, stream);
+    if (p.head_dim == 64)
+        return pairs ? launch_impl<64, 16, true>(p, tk, tv, grid, stream)
+                     : launch_impl<64, 16, false>(p, tk, tv, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -65,7 +65,7 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     const int b = blockIdx.z;
     const int rows = min(kRowsPerTile, p.group - tile * kRowsPerTile);
     const SeqWork w = seq_work(p, b, part);
-    if (w.blk_begin >= w.blk_end) {
+    if (w.tok_begin >= w.tok_end) {
         write_empty<D>(p, b, g, tile, part, rows, w.nparts);
         return;
     }
@@ -91,8 +91,8 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     const KV *kc = static_cast<const KV *>(p.k_cache);
     const KV *vc = static_cast<const KV *>(p.v_cache);
     const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
-    const int t_begin = w.blk_begin * p.block_size;
-    const int t_end = min(w.len, w.blk_end * p.block_size);
+    const int t_begin = w.tok_begin;
+    const int t_end = w.tok_end;
     for (int t = t_begin + warp; t < t_end; t += kWarps) {
         const int64_t phys = table[t / p.block_size];
         float kx[E], vx[E];

@@ -46,7 +46,7 @@ struct DecodeParams {
     int cluster_merge;   // fused split merged through distributed shared memory
                          // (grid.x = nsplit = cluster size)
     int nsplit;          // grid.x: partitions per (sequence, head tile)
-    int part_blocks;     // blocks per partition
+    int part_tokens;     // tokens per partition (a multiple of the kernel's tile length)
     int mode;
     int out_bf16;
     int q_bf16;
@@ -239,11 +239,10 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
 // Per-sequence bookkeeping shared by every decode kernel
 // ---------------------------------------------------------------------------
 struct SeqWork {
-    int len;        // tokens attended (clamped to the table's capacity)
-    int nblk;       // blocks holding those tokens
+    int len;        // tokens attended (clamped to the cache's capacity and the grid's reach)
     int nparts;     // partitions with work (fused / final modes)
-    int blk_begin;  // this CTA's first block
-    int blk_end;    // one past its last block
+    int tok_begin;  // this CTA's first token
+    int tok_end;    // one past its last token (<= tok_begin: nothing to do)
 };
 
 __device__ __forceinline__ SeqWork seq_work(const DecodeParams &p, int b, int part) {
@@ -252,18 +251,12 @@ __device__ __forceinline__ SeqWork seq_work(const DecodeParams &p, int b, int pa
     if (len < 0) len = 0;
     const int cap = p.contig_stride > 0 ? p.contig_stride : p.max_blocks * p.block_size;
     if (len > cap) len = cap;
-    int nblk = (len + p.block_size - 1) / p.block_size;
-    int nparts = (nblk + p.part_blocks - 1) / p.part_blocks;
-    if (nparts > p.nsplit) {
-        nparts = p.nsplit;
-        nblk = nparts * p.part_blocks;
-        len = nblk * p.block_size;
-    }
+    const int64_t reach = static_cast<int64_t>(p.nsplit) * p.part_tokens;
+    if (len > reach) len = static_cast<int>(reach);
     w.len = len;
-    w.nblk = nblk;
-    w.nparts = nparts;
-    w.blk_begin = part * p.part_blocks;
-    w.blk_end = min(nblk, w.blk_begin + p.part_blocks);
+    w.nparts = (len + p.part_tokens - 1) / p.part_tokens;
+    w.tok_begin = part * p.part_tokens;
+    w.tok_end = min(len, w.tok_begin + p.part_tokens);
     return w;
 }
 

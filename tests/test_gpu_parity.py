@@ -67,10 +67,12 @@ def test_decode_small(case, use_ws):
     assert_clean_status()
 
 
-def test_decode_nan_in_unused_slots_and_table_tail():
+@pytest.mark.parametrize("bs", [16, 8])
+def test_decode_nan_in_unused_slots_and_table_tail(bs):
     """Slots past a context and table entries past its blocks hold garbage:
-    neither may reach the output."""
-    lens, Hq, Hkv, D, bs = (5, 17, 40), 8, 2, 128, 16
+    neither may reach the output (blocks of 8: a 16-token tile whose second
+    block lies past the context must not read that block's table entry)."""
+    lens, Hq, Hkv, D = (5, 17, 40), 8, 2, 128
     batch = workloads.make_batch("nan", lens, Hq, Hkv, D, bs, 32, True, seed_values=7)
     k, v = batch.k_cache, batch.v_cache
     for b, n in enumerate(lens):
@@ -125,7 +127,7 @@ def test_decode_bf16_output():
 # ---------------------------------------------------------------------------
 # split-K partitions and the log-sum-exp merge
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("bs,ps", [(16, 512), (8, 64), (32, 96), (16, 48)])
+@pytest.mark.parametrize("bs,ps", [(16, 512), (8, 64), (32, 96), (16, 48), (8, 24)])
 def test_splitk_partitions_and_merge(bs, ps):
     lens = (1, 100, 511, 512, 513, 1500)
     Hq, Hkv, D = 16, 4, 128

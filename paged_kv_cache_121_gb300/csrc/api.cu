@@ -106,18 +106,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 4-D view of a bf16 cache [num_blocks, block_size, Hkv, D] (innermost first:
-// D, Hkv, block_size, num_blocks); box = 64 dims x 1 head x box_tokens tokens
-// x 1 block, 128-byte swizzle. Out-of-range block ids read as zeros.
+// 4-D view of a bf16 cache [num_blocks, block_size, Hkv, D], listed innermost
+// first as (D, token, head, block) -- the token and head strides swapped, so
+// that a box of 64 dims x box_tokens tokens x box_heads heads lands in shared
+// memory head by head, each head's rows contiguous. 128-byte swizzle;
+// out-of-range coordinates read as zeros.
 pa_status make_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int64_t block_size,
-                         int num_kv_heads, int head_dim, int box_tokens) {
+                         int num_kv_heads, int head_dim, int box_tokens, int box_heads) {
     auto enc = tensor_map_encoder();
     if (!enc) return PA_ERR_CUDA;
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
-                                static_cast<cuuint64_t>(block_size), static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
+                                static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
-    const cuuint64_t strides[3] = {row, row * num_kv_heads, row * num_kv_heads * block_size};
-    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_tokens), 1};
+    const cuuint64_t strides[3] = {row * num_kv_heads, row, row * num_kv_heads * block_size};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_tokens), static_cast<cuuint32_t>(box_heads), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -278,6 +280,8 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
     cudaError_t e;
     if (mma) {
         const int box = decode_mma_box_tokens(s.block_size);
+        // one box covers every head of the CTA (blocks of 8: one head per box)
+        const int box_heads = s.block_size < decode_mma_tile_tokens(s.block_size) ? 1 : p.heads_per_cta;
         const int stage = decode_mma_stage_bytes(s.head_dim, s.block_size, p.heads_per_cta);
         p.ring_bytes = std::max(stage, (ring_kb() * 1024) / stage * stage);
         if (p.cluster_merge) {
@@ -289,9 +293,9 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
         const int64_t map_blocks = contig ? 1 : s.num_blocks;
         const int64_t map_tokens = contig ? static_cast<int64_t>(s.num_seqs) * p.contig_stride : s.block_size;
         CUtensorMap tk, tv;
-        pa_status st = make_cache_map(&tk, p.k_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box);
+        pa_status st = make_cache_map(&tk, p.k_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box, box_heads);
         if (st != PA_OK) return st;
-        st = make_cache_map(&tv, p.v_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box);
+        st = make_cache_map(&tv, p.v_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box, box_heads);
         if (st != PA_OK) return st;
         e = launch_decode_mma(p, tk, tv, grid, stream);
     } else {

@@ -106,22 +106,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 4-D view of a bf16 cache [num_blocks, block_size, Hkv, D], listed innermost
-// first as (D, token, head, block) -- the token and head strides swapped, so
-// that a box of 64 dims x box_tokens tokens x box_heads heads lands in shared
-// memory head by head, each head's rows contiguous. 128-byte swizzle;
-// out-of-range coordinates read as zeros.
+// 5-D view of a bf16 cache [num_blocks, block_size, Hkv, D], listed innermost
+// first as (dim within a 64-dim half, token, half, head, block): the strides
+// of the middle three are permuted so that a box of 64 dims x box_tokens
+// tokens x every half x box_heads heads lands in shared memory as
+// [head][half][token][128 bytes]. 128-byte swizzle; out-of-range
+// coordinates read as zeros.
 pa_status make_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int64_t block_size,
                          int num_kv_heads, int head_dim, int box_tokens, int box_heads) {
     auto enc = tensor_map_encoder();
     if (!enc) return PA_ERR_CUDA;
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(block_size),
+    const cuuint64_t halves = static_cast<cuuint64_t>(head_dim / 64);
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(block_size), halves,
                                 static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
-    const cuuint64_t strides[3] = {row * num_kv_heads, row, row * num_kv_heads * block_size};
-    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_tokens), static_cast<cuuint32_t>(box_heads), 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims, strides,
+    const cuuint64_t strides[4] = {row * num_kv_heads, 128, row, row * num_kv_heads * block_size};
+    const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(box_tokens), static_cast<cuuint32_t>(halves),
+                               static_cast<cuuint32_t>(box_heads), 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
@@ -280,8 +283,7 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
     cudaError_t e;
     if (mma) {
         const int box = decode_mma_box_tokens(s.block_size);
-        // one box covers every head of the CTA (blocks of 8: one head per box)
-        const int box_heads = s.block_size < decode_mma_tile_tokens(s.block_size) ? 1 : p.heads_per_cta;
+        const int box_heads = p.heads_per_cta;     // one box covers every head of the CTA
         const int stage = decode_mma_stage_bytes(s.head_dim, s.block_size, p.heads_per_cta);
         p.ring_bytes = std::max(stage, (ring_kb() * 1024) / stage * stage);
         if (p.cluster_merge) {

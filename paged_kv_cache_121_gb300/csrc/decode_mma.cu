@@ -47,8 +47,9 @@ struct MmaCfg {
     static constexpr int kHalves = D / 64;
     static constexpr int kHalfBytes = TT * 128;         // one 64-dim half of one head's tile
     static constexpr int kHeadBytes = TT * D * 2;       // one head's K (or V) rows of a tile
-    // Stage layout, K then V: [64-dim half][head][token][128 bytes], so one
-    // TMA box (64 dims x TT tokens x every head of the CTA) fills a half.
+    // Stage layout, K then V: [head][64-dim half][token][128 bytes], filled by
+    // one TMA box (64 dims x TT tokens x every half x every head of the CTA).
+    // Blocks of TT / 2 tokens: [block of the pair][head][half][token].
     static constexpr int kMaxRingBytes = 200 * 1024;
     static constexpr int kMaxStages = 32;
     static constexpr size_t kBarrierBytes = 2 * kMaxStages * sizeof(uint64_t);
@@ -359,7 +360,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int nstages = p.ring_bytes / stage_bytes;
     if (nstages > C::kMaxStages) nstages = C::kMaxStages;
     const int v_off = hpc * C::kHeadBytes;
-    const int half_stride = hpc * C::kHalfBytes;   // bytes between the 64-dim halves of K (or V)
+    // byte offsets within one stage's K (or V): head, 64-dim half, token row
+    constexpr int kHalfStride = box_rows * 128;
+    constexpr int kHeadStride = C::kHalves * kHalfStride;
+    const int pair_stride = hpc * kHeadStride;     // second block of a pair
+    auto tok_off = [&](int t) -> int {
+        return kPairs ? (t / box_rows) * pair_stride + (t % box_rows) * 128 : t * 128;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
@@ -431,32 +438,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const uint32_t kdst = smem_addr(smem + s * stage_bytes);
                     const int tok0 = contig ? contig_tok0 + i * TT : t0 % bs;
                     const int blk0 = contig ? 0 : phys0;
-                    // tensor-map coordinates, innermost first: (dim, token, head, block)
-                    if constexpr (!kPairs) {
-                        // one box per half covers every head of the CTA
-#pragma unroll
-                        for (int hh = 0; hh < C::kHalves; ++hh) {
-                            const uint32_t off = hh * half_stride;
-                            tma_load_4d(kdst + off, &tmap_k, hh * 64, tok0, head0, blk0, full, policy);
-                            tma_load_4d(kdst + v_off + off, &tmap_v, hh * 64, tok0, head0, blk0, full, policy);
-                        }
-                    } else {
-                        // one-head boxes of one block: the tile's two blocks land back to back
-                        for (int h = 0; h < hpc; ++h) {
-#pragma unroll
-                            for (int hh = 0; hh < C::kHalves; ++hh) {
-                                const uint32_t off = hh * half_stride + h * C::kHalfBytes;
-                                tma_load_4d(kdst + off, &tmap_k, hh * 64, 0, head0 + h, blk0, full, policy);
-                                tma_load_4d(kdst + v_off + off, &tmap_v, hh * 64, 0, head0 + h, blk0, full,
-                                            policy);
-                                if (nbox > 1) {
-                                    const uint32_t off1 = off + box_rows * 128;
-                                    tma_load_4d(kdst + off1, &tmap_k, hh * 64, 0, head0 + h, phys1, full, policy);
-                                    tma_load_4d(kdst + v_off + off1, &tmap_v, hh * 64, 0, head0 + h, phys1, full,
-                                                policy);
-                                }
-                            }
-                        }
+                    // tensor-map coordinates, innermost first: (dim, token, half, head, block);
+                    // one box of K and one of V per block
+                    tma_load_5d(kdst, &tmap_k, 0, tok0, 0, head0, blk0, full, policy);
+                    tma_load_5d(kdst + v_off, &tmap_v, 0, tok0, 0, head0, blk0, full, policy);
+                    if (kPairs && nbox > 1) {
+                        tma_load_5d(kdst + pair_stride, &tmap_k, 0, 0, 0, head0, phys1, full, policy);
+                        tma_load_5d(kdst + v_off + pair_stride, &tmap_v, 0, 0, 0, head0, phys1, full, policy);
                     }
                     issued = i + 1;
                 }
@@ -495,7 +483,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 s_abort = 1;
                 break;
             }
-            unsigned char *kst = smem + s * stage_bytes + warp * C::kHalfBytes;   // this head, half 0
+            unsigned char *kst = smem + s * stage_bytes + warp * kHeadStride;   // this head
             const uint32_t kbase = smem_addr(kst);
             const uint32_t vbase = kbase + v_off;
             const int valid = min(TT, tok_end - (tok_begin + i * TT));
@@ -504,7 +492,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int c = lane; c < C::kHalves * TT * 8; c += 32) {
                     const int hh = c / (TT * 8), row = (c % (TT * 8)) / 8;
                     if (row >= valid)
-                        reinterpret_cast<uint4 *>(kst + v_off + hh * half_stride)[c % (TT * 8)] =
+                        *reinterpret_cast<uint4 *>(kst + v_off + hh * kHalfStride + tok_off(row) + (c % 8) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                 }
                 __syncwarp();
@@ -520,7 +508,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int kk = 0; kk < D / 16; kk += 2) {
                     const int tok = 8 * j + (lane & 7);
                     const int c = 2 * kk + (lane >> 3);
-                    const uint32_t addr = kbase + (c >> 3) * half_stride + tok * 128 +
+                    const uint32_t addr = kbase + (c >> 3) * kHalfStride + tok_off(tok) +
                                           (((c & 7) ^ (tok & 7)) << 4);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(addr, b0, b1, b2, b3);
@@ -590,7 +578,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int mi = lane >> 3;
                 const int tok = (mi & 1) * 8 + (lane & 7);
                 const int c = dn + (mi >> 1);
-                const uint32_t addr = vbase + (c >> 3) * half_stride + tok * 128 +
+                const uint32_t addr = vbase + (c >> 3) * kHalfStride + tok_off(tok) +
                                       (((c & 7) ^ (tok & 7)) << 4);
                 uint32_t v0, v1, v2, v3;
                 ldmatrix_x4_trans(addr, v0, v1, v2, v3);

@@ -512,8 +512,10 @@ def run_ours(args, rank, world, local_rank):
     traffic = profiled_traffic(args.config) if headline else None
     if contig:
         kernel = "decode_mma_kernel<128,16> (contiguous)"
-    elif bs in (8, 16, 32, 64, 128, 256):
-        kernel = "decode_mma_kernel<128,%d>" % min(bs, 16)
+    elif bs == 8:
+        kernel = "decode_mma_kernel<128,16> (two blocks per tile)"
+    elif bs in (16, 32, 64, 128, 256):
+        kernel = "decode_mma_kernel<128,16>"
     else:
         kernel = "decode_simt_kernel"
     decode_launches = plan["kernel_launches"]       # a wide split adds the merge kernel

@@ -167,6 +167,45 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
                            size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Decode attention for a batch whose sequences share their leading blocks.
+ * [P1] "Copy-on-write: when two requests share a prefix" (several block
+ * tables point at the same physical blocks, reference-counted); [P5]
+ * "Sharing a prefix: one copy for many requests" (the prefix is stored
+ * once). pa_decode reads a shared block once per sequence; this entry point
+ * reads it once for the whole batch: the shared tokens are attended for
+ * every (sequence, query head) row by one pass, the rest of each context by
+ * the paged decode kernel, and the two are merged by log-sum-exp. The result
+ * is pa_decode's (the same softmax over the same tokens).
+ *
+ *   shared_blocks  the number of leading block-table entries that are the
+ *                  same physical blocks in every row of block_tables, and
+ *                  full: every context_len >= shared_blocks * block_size.
+ *                  (Not checked on the device. Rows that differ give that
+ *                  row's wrong answer, never an out-of-bounds access.)
+ *                  Shared tokens are taken in whole 16-token tiles (blocks
+ *                  of 8: an odd last shared block is attended with the rest).
+ *   workspace      at least pa_decode_shared_prefix_workspace_size() bytes
+ *                  (required: the two passes meet there). Its contents need
+ *                  no initialisation; calls sharing it must not overlap.
+ *   Other arguments as pa_decode. Supported: bf16 query and cache, head_dim
+ *   64 or 128, block_size 8, 16, 32, 64, 128 or 256. With no whole tile
+ *   shared this is pa_decode.
+ * ---------------------------------------------------------------------- */
+PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                                     int head_dim, int block_size,
+                                                     int max_context_len, int shared_blocks);
+
+PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const void *query,
+                                         pa_dtype q_dtype, const void *k_cache,
+                                         const void *v_cache, pa_dtype kv_dtype,
+                                         const int32_t *block_tables, const int32_t *context_lens,
+                                         int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int max_blocks_per_seq,
+                                         int num_blocks, int max_context_len, int shared_blocks,
+                                         float scale, void *workspace, size_t workspace_bytes,
+                                         void *stream);
+
+/* ------------------------------------------------------------------------
  * Decode attention over a contiguous (unpaged) cache: the baseline that
  * paging is measured against.
  * [P5] "The problem: reserving the maximum" (one buffer per request, sized

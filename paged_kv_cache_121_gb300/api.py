@@ -126,6 +126,28 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, max_cont
                                 _stream(stream)), "pa_decode")
 
 
+def pa_decode_shared_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                           max_context_len, shared_blocks) -> int:
+    return int(_lib.load().pa_decode_shared_prefix_workspace_size(
+        num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, shared_blocks))
+
+
+def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                            shared_blocks, scale, workspace, stream=None) -> None:
+    """Decode attention where the first ``shared_blocks`` entries of every
+    block-table row are the same (full) physical blocks: they are read once
+    for the whole batch. ``workspace``: a uint8 tensor of at least
+    :func:`pa_decode_shared_prefix_workspace_size` bytes."""
+    nb, bs, hkv, d = _cache_dims(k_cache)
+    B, hq, _ = (int(x) for x in query.shape)
+    ws_bytes = int(workspace.numel() * workspace.element_size()) if workspace is not None else 0
+    _check(_lib.load().pa_decode_shared_prefix(
+        _ptr(out), _dtype(out), _ptr(query), _dtype(query), _ptr(k_cache), _ptr(v_cache), _dtype(k_cache),
+        _ptr(block_tables), _ptr(context_lens), B, hq, hkv, d, bs, int(block_tables.shape[1]), nb,
+        int(max_context_len), int(shared_blocks), float(scale), _ptr(workspace), ws_bytes, _stream(stream)),
+        "pa_decode_shared_prefix")
+
+
 def pa_decode_contiguous(out, query, k, v, context_lens, max_context_len, scale, workspace=None,
                          stream=None) -> None:
     """Decode attention over a contiguous cache ``k``, ``v`` [B, max_seq_len,

@@ -30,6 +30,7 @@ constexpr int kMmaHeadsPerCta = 4;    // KV heads per tensor-core CTA (consumer 
 constexpr int kContiguousTile = 16;   // tokens per tile of a contiguous cache
 constexpr int kMmaRingKiB = 96;       // shared-memory ring per tensor-core CTA
 constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
+constexpr int kMinPrefixChunk = 64;   // tokens per chunk of the shared-prefix pass, at least
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int *> g_status_addr[kMaxDevices];
@@ -356,7 +357,7 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
     p.part_tokens = pl.part_tokens;
     p.cluster_merge = pl.cluster ? 1 : 0;
     if (pl.cluster) {
-        p.mode = kModeFused;
+        p.mode = kModeFinal;   // the cluster merge writes the output
     } else if (pl.nsplit > 1) {
         const WorkspaceLayout wl = workspace_layout(s, pl);
         if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
@@ -366,6 +367,65 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
         p.mode = kModeFinal;
     }
     return launch_decode(s, p, kv_dtype, pl.mma, dev, as_stream(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Shared-prefix decode: the shared leading blocks attended once for every row
+// (prefix pass), the rest of each context by the decode kernel in split-K
+// form, both merged by the log-sum-exp merge.
+// ---------------------------------------------------------------------------
+struct PrefixPlan {
+    int prefix_tokens;   // shared tokens attended by the prefix pass (a multiple of 16)
+    int chunk_tokens;
+    int chunks;          // prefix partitions (grid.x of the prefix pass)
+    int row_groups;      // grid.z of the prefix pass
+    Plan suffix;         // the decode kernel's split of the rest (never a cluster)
+    int part_stride;     // partitions per (sequence, head): chunks + suffix splits
+};
+
+PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms) {
+    PrefixPlan pp{};
+    int64_t P = std::min<int64_t>(static_cast<int64_t>(shared_blocks) * s.block_size, s.max_ctx);
+    P = P / 16 * 16;   // whole 16-token tiles (blocks of 8: an odd last block goes to the rest)
+    pp.prefix_tokens = static_cast<int>(P);
+    const int group = s.num_heads / s.num_kv_heads;
+    pp.row_groups = static_cast<int>(cdiv64(static_cast<int64_t>(s.num_seqs) * group, prefix_rows_per_cta()));
+    if (P > 0) {
+        const int64_t per_chunk = static_cast<int64_t>(s.num_kv_heads) * pp.row_groups;
+        const int64_t cap = static_cast<int64_t>(sms) * kCtasPerSmMma;
+        int64_t chunks = std::max<int64_t>(1, cap / per_chunk);
+        chunks = std::min<int64_t>(chunks, std::max<int64_t>(1, P / kMinPrefixChunk));
+        chunks = std::min<int64_t>(chunks, kMaxSplits);
+        const int64_t tiles = P / 16;
+        const int64_t ct = cdiv64(tiles, chunks);
+        pp.chunk_tokens = static_cast<int>(ct * 16);
+        pp.chunks = static_cast<int>(cdiv64(tiles, ct));
+    }
+    DecodeShape rest = s;
+    rest.max_ctx = static_cast<int>(std::max<int64_t>(0, s.max_ctx - P));
+    pp.suffix = plan_split(rest, sms, true);
+    pp.suffix.cluster = false;
+    pp.part_stride = pp.chunks + pp.suffix.nsplit;
+    return pp;
+}
+
+WorkspaceLayout prefix_workspace(const DecodeShape &s, const PrefixPlan &pp) {
+    WorkspaceLayout w{};
+    const size_t rows = static_cast<size_t>(s.num_seqs) * s.num_heads * pp.part_stride;
+    w.o_off = 0;
+    w.ml_off = align256(rows * s.head_dim * sizeof(float));
+    w.count_off = w.ml_off + align256(rows * sizeof(float));
+    w.total = w.count_off + align256(rows * sizeof(float));
+    return w;
+}
+
+pa_status check_prefix_call(const DecodeShape &s, pa_dtype q_dtype, pa_dtype kv_dtype, int shared_blocks) {
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
+    if (shared_blocks < 0 || shared_blocks > s.max_blocks) return PA_ERR_INVALID_ARG;
+    if (kv_dtype != PA_BF16 || !decode_mma_supported(s.head_dim, s.block_size)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
 }
 
 }  // namespace
@@ -524,6 +584,110 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
     if (!block_tables) return PA_ERR_INVALID_ARG;
     return decode_planned(s, out, out_dtype, query, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
                           context_lens, 0, scale, workspace, workspace_bytes, stream);
+}
+
+PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                                     int head_dim, int block_size, int max_context_len,
+                                                     int shared_blocks) {
+    const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        std::max(1, block_size > 0 ? (max_context_len + block_size - 1) / block_size : 1),
+                        1, max_context_len};
+    if (check_prefix_call(s, PA_BF16, PA_BF16, std::min(shared_blocks, s.max_blocks)) != PA_OK) return 0;
+    int dev;
+    if (current_device(&dev) != PA_OK) return 0;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return 0;
+    const PrefixPlan pp = plan_prefix(s, shared_blocks, sms);
+    const size_t plain = workspace_layout(s, plan_split(s, sms, true)).total;
+    return std::max(prefix_workspace(s, pp).total, plain);
+}
+
+PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
+                                         const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
+                                         const int32_t *block_tables, const int32_t *context_lens,
+                                         int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                         int block_size, int max_blocks_per_seq, int num_blocks,
+                                         int max_context_len, int shared_blocks, float scale, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
+    const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        max_blocks_per_seq, num_blocks, max_context_len};
+    pa_status st = check_prefix_call(s, q_dtype, kv_dtype, shared_blocks);
+    if (st != PA_OK) return st;
+    if (!valid_dtype(out_dtype) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    int dev;
+    if ((st = current_device(&dev)) != PA_OK) return st;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PA_ERR_CUDA;
+    const PrefixPlan pp = plan_prefix(s, shared_blocks, sms);
+    if (pp.chunks == 0)   // nothing shared in whole tiles: the plain decode
+        return decode_planned(s, out, out_dtype, query, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                              context_lens, 0, scale, workspace, workspace_bytes, stream);
+    const WorkspaceLayout wl = prefix_workspace(s, pp);
+    if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+    int *status = status_word(dev);
+    if (!status) return PA_ERR_CUDA;
+    char *ws = static_cast<char *>(workspace);
+    float *tmp_out = reinterpret_cast<float *>(ws + wl.o_off);
+    float *max_logits = reinterpret_cast<float *>(ws + wl.ml_off);
+    float *exp_sums = reinterpret_cast<float *>(ws + wl.count_off);
+    cudaStream_t strm = as_stream(stream);
+
+    // 1. the shared prefix, once for every row
+    PrefixParams pq;
+    std::memset(&pq, 0, sizeof pq);
+    pq.query = query;
+    pq.prefix_table = block_tables;   // row 0 holds the shared ids like every row
+    pq.context_lens = context_lens;
+    pq.tmp_out = tmp_out;
+    pq.max_logits = max_logits;
+    pq.exp_sums = exp_sums;
+    pq.status = status;
+    pq.num_seqs = num_seqs;
+    pq.num_heads = num_heads;
+    pq.num_kv_heads = num_kv_heads;
+    pq.head_dim = head_dim;
+    pq.group = num_heads / num_kv_heads;
+    pq.block_size = block_size;
+    pq.prefix_tokens = pp.prefix_tokens;
+    pq.chunk_tokens = pp.chunk_tokens;
+    pq.part_stride = pp.part_stride;
+    const int stage = prefix_stage_bytes(head_dim);
+    pq.ring_bytes = std::max(stage, std::min(kPrefixMaxRingBytes, ring_kb() * 1024) / stage * stage);
+    pq.scale_log2 = scale * kLog2e;
+    {
+        const int box = decode_mma_box_tokens(block_size);
+        CUtensorMap tk, tv;
+        if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK)
+            return st;
+        if ((st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK)
+            return st;
+        const dim3 grid(static_cast<unsigned>(pp.chunks), static_cast<unsigned>(num_kv_heads),
+                        static_cast<unsigned>(pp.row_groups));
+        if (launch_prefix_mma(pq, tk, tv, grid, strm) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    // 2. the rest of every context, split-K partitions after the prefix chunks
+    DecodeParams p;
+    fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.ntile = pp.suffix.ntile;
+    p.heads_per_cta = pp.suffix.heads_per_cta;
+    p.nsplit = pp.suffix.nsplit;
+    p.part_tokens = pp.suffix.part_tokens;
+    p.skip_tokens = pp.prefix_tokens;
+    p.part_stride = pp.part_stride;
+    p.part_offset = pp.chunks;
+    p.mode = kModeSplitK;
+    if ((st = launch_decode(s, p, kv_dtype, true, dev, strm)) != PA_OK) return st;
+    // 3. merge all partitions of every row
+    const cudaError_t e = launch_lse_merge(out, out_dtype == PA_BF16 ? 1 : 0, tmp_out, max_logits, exp_sums,
+                                           context_lens, num_seqs, num_heads, head_dim, pp.part_stride, 0, strm);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_API pa_status pa_decode_contiguous(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,

@@ -11,13 +11,15 @@
 // 16 tokens; a block of 32 or more tokens may straddle two partitions).
 //  * The last warp walks the block table (read 32 tiles' entries at a time, a
 //    chunk ahead) and, per 16-token tile (two blocks when blocks are 8 tokens),
-//    issues TMA tiled loads (cp.async.bulk.tensor) of the tile's K and V rows
-//    for every KV head of the group into one stage of a shared-memory ring;
-//    completion is counted on the stage's mbarrier. All heads of a block are
-//    requested back to back, so each block's K (and V) -- contiguous in the
-//    [num_blocks, block_size, Hkv, D] layout -- is fetched as one burst.
-//    Rows land as 64-dim halves with the 128-byte swizzle, which makes the
-//    matrix loads below bank-conflict free.
+//    issues one TMA tiled load (cp.async.bulk.tensor.5d) of the tile's K and
+//    one of its V into a stage of a shared-memory ring; completion is counted
+//    on the stage's mbarrier. The tensor map views the cache as (dim within a
+//    64-dim half, token, half, head, block), so one box covers every KV head
+//    of the group and both halves: the block's K (and V) -- contiguous in the
+//    [num_blocks, block_size, Hkv, D] layout -- is fetched as one burst, and
+//    the producer issues two instructions per tile. Rows land head by head
+//    as 64-dim halves with the 128-byte swizzle, which makes the matrix loads
+//    below bank-conflict free.
 //  * Consumer warp j owns KV head j of the group for the whole CTA and reads
 //    every stage. S = Q K^T runs on the tensor cores (mma.m16n8k16, M = the
 //    query heads of the GQA group, N = tokens, K = head dims; Q stays in
@@ -28,15 +30,15 @@
 //    every head's warp has released it.
 //  * Tokens past the context in the last tile are masked (score -inf, V rows
 //    zeroed in shared memory, so stale or NaN slot contents never leak).
-//  * Each warp finishes its own head from registers: the final output, a
-//    split-K partition, or (fused split) its partition followed by an
-//    arrival count; the last partition to arrive merges them by log-sum-exp.
+//  * Each warp finishes its own head from registers: the final output or a
+//    split-K partition (merged by the log-sum-exp merge kernel); or, when a
+//    context's partitions form one thread-block cluster, the partitions are
+//    merged through distributed shared memory.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the device status word, drains its own copies and returns.
-#include <type_traits>
-
 #include "device_common.cuh"
 #include "internal.h"
+#include "mma_tile.cuh"
 
 namespace pa {
 
@@ -58,15 +60,6 @@ struct MmaCfg {
     static_assert(TT == 16, "tiles are 16 tokens (two 8-token blocks, or part of a larger block)");
 };
 
-constexpr float kRescaleSlack = 8.f;   // base-2 headroom before the running max is moved
-
-__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &hi, uint32_t &lo) {
-    hi = pack_bf16x2(x, y);
-    const float hx = bf16_bits_to_float(hi & 0xffffu);
-    const float hy = bf16_bits_to_float(hi >> 16);
-    lo = pack_bf16x2(x - hx, y - hy);
-}
-
 __device__ __forceinline__ void store_out2(const DecodeParams &p, int64_t idx, float a, float c) {
     if (p.out_bf16)
         *reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(p.out) + idx) = pack_bf16x2(a, c);
@@ -74,30 +67,15 @@ __device__ __forceinline__ void store_out2(const DecodeParams &p, int64_t idx, f
         *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + idx) = make_float2(a, c);
 }
 
-__device__ __forceinline__ float vec_get(const float4 &v, int e) {
-    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-}
-__device__ __forceinline__ float vec_get(const float2 &v, int e) { return e == 0 ? v.x : v.y; }
 
-// One warp's softmax state for 16 query rows of one KV head, in the mma
-// accumulator layout: lane (r = lane/4, q = lane%4) holds rows r and r+8,
-// dims 8*dn + 2q and +1 of every 8-dim slice dn.
+// Write a warp's result (final output or split-K partition) for query heads
+// h0 .. h0+rows-1.
 template <int D>
-struct WarpState {
-    float o[D / 8][4];
-    float m0, m1, l0, l1;   // reference max (base 2) and sum of 2^(s - m) per row
-    float t0, t1;           // true running max of the scores (base 2)
-};
-
-// Write a warp's result (final output, split-K partition, or fused partition
-// + last-arrival merge) for query heads h0 .. h0+rows-1.
-template <int D>
-__device__ __forceinline__ void warp_epilogue(const DecodeParams &p, WarpState<D> &st, int b, int gh, int tile,
-                              int part, int h0, int rows, int nparts, int lane) {
+__device__ __forceinline__ void warp_epilogue(const DecodeParams &p, WarpState<D> &st, int b, int part,
+                                              int h0, int rows, int lane) {
     const int r = lane >> 2, q4 = lane & 3;
-    const int mode = (p.mode == kModeFused && nparts <= 1) ? kModeFinal : p.mode;
     const bool v0 = r < rows, v1 = r + 8 < rows;
-    if (mode == kModeFinal) {
+    if (p.mode == kModeFinal) {
         const float i0 = st.l0 > 0.f ? 1.f / st.l0 : 0.f, i1 = st.l1 > 0.f ? 1.f / st.l1 : 0.f;
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn) {
@@ -109,126 +87,25 @@ __device__ __forceinline__ void warp_epilogue(const DecodeParams &p, WarpState<D
         }
         return;
     }
-    const int S = p.nsplit;
-    const int64_t row0 = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S + part;
-    const int64_t row1 = row0 + 8 * static_cast<int64_t>(S);
-    if (mode == kModeSplitK) {
-        const float i0 = st.l0 > 0.f ? 1.f / st.l0 : 0.f, i1 = st.l1 > 0.f ? 1.f / st.l1 : 0.f;
-#pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn) {
-            const int d = 8 * dn + 2 * q4;
-            if (v0) *reinterpret_cast<float2 *>(p.tmp_out + row0 * D + d) = make_float2(st.o[dn][0] * i0, st.o[dn][1] * i0);
-            if (v1) *reinterpret_cast<float2 *>(p.tmp_out + row1 * D + d) = make_float2(st.o[dn][2] * i1, st.o[dn][3] * i1);
-        }
-        if (q4 == 0) {   // report the true max: sum of 2^(s - t) = l * 2^(m - t)
-            if (v0) {
-                p.max_logits[row0] = st.l0 > 0.f ? st.t0 * kLn2 : -INFINITY;
-                p.exp_sums[row0] = st.l0 > 0.f ? st.l0 * fast_exp2(st.m0 - st.t0) : 0.f;
-            }
-            if (v1) {
-                p.max_logits[row1] = st.l1 > 0.f ? st.t1 * kLn2 : -INFINITY;
-                p.exp_sums[row1] = st.l1 > 0.f ? st.l1 * fast_exp2(st.m1 - st.t1) : 0.f;
-            }
-        }
-        return;
-    }
-    // fused: publish this partition (unnormalised), count arrivals, last one merges
+    const int64_t row0 = split_row(p, b, h0 + r, part);
+    const int64_t row1 = split_row(p, b, h0 + r + 8, part);
+    const float i0 = st.l0 > 0.f ? 1.f / st.l0 : 0.f, i1 = st.l1 > 0.f ? 1.f / st.l1 : 0.f;
 #pragma unroll
     for (int dn = 0; dn < D / 8; ++dn) {
         const int d = 8 * dn + 2 * q4;
-        if (v0) *reinterpret_cast<float2 *>(p.ws_o + row0 * D + d) = make_float2(st.o[dn][0], st.o[dn][1]);
-        if (v1) *reinterpret_cast<float2 *>(p.ws_o + row1 * D + d) = make_float2(st.o[dn][2], st.o[dn][3]);
+        if (v0) *reinterpret_cast<float2 *>(p.tmp_out + row0 * D + d) = make_float2(st.o[dn][0] * i0, st.o[dn][1] * i0);
+        if (v1) *reinterpret_cast<float2 *>(p.tmp_out + row1 * D + d) = make_float2(st.o[dn][2] * i1, st.o[dn][3] * i1);
     }
-    if (q4 == 0) {
-        if (v0) *reinterpret_cast<float2 *>(p.ws_ml + row0 * 2) = make_float2(st.m0, st.l0);
-        if (v1) *reinterpret_cast<float2 *>(p.ws_ml + row1 * 2) = make_float2(st.m1, st.l1);
-    }
-    __threadfence();
-    __syncwarp();
-    unsigned *counter = p.ws_count + (static_cast<int64_t>(b) * p.num_kv_heads + gh) * p.ntile + tile;
-    unsigned last = 0;
-    if (lane == 0) last = atomicAdd(counter, 1u) == static_cast<unsigned>(nparts - 1) ? 1u : 0u;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
-    // Merge, two query rows at a time. Each lane owns D/32 consecutive dims and
-    // reads them as one vector per (row, partition); lane j also reads the
-    // (max, sum) of partition j (and j + 32). All those loads are issued
-    // before any of them is used, so the whole merge costs about one L2 round
-    // trip per chunk of kMergeChunk partitions instead of one per partition.
-    constexpr int kVec = D / 32;
-    using VecT = typename std::conditional<kVec == 4, float4, float2>::type;
-    constexpr int kMergeChunk = 12;
-    for (int rg = 0; rg < rows; rg += 2) {
-        const bool live1 = rg + 1 < rows;
-        const int64_t base0 = (static_cast<int64_t>(b) * p.num_heads + h0 + rg) * S;
-        const int64_t base1 = base0 + S;
-        float2 mla[2], mlb[2];
-        mla[0] = mla[1] = mlb[0] = mlb[1] = make_float2(-INFINITY, 0.f);
-        if (lane < nparts) {
-            mla[0] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + (base0 + lane) * 2));
-            if (live1) mla[1] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + (base1 + lane) * 2));
+    if (q4 == 0) {   // report the true max: sum of 2^(s - t) = l * 2^(m - t)
+        if (v0) {
+            p.max_logits[row0] = st.l0 > 0.f ? st.t0 * kLn2 : -INFINITY;
+            p.exp_sums[row0] = st.l0 > 0.f ? st.l0 * fast_exp2(st.m0 - st.t0) : 0.f;
         }
-        if (lane + 32 < nparts) {
-            mlb[0] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + (base0 + lane + 32) * 2));
-            if (live1) mlb[1] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + (base1 + lane + 32) * 2));
-        }
-        const VecT *src0 = reinterpret_cast<const VecT *>(p.ws_o + base0 * D) + lane;
-        const VecT *src1 = reinterpret_cast<const VecT *>(p.ws_o + base1 * D) + lane;
-        constexpr int kStride = D / kVec;   // VecT elements per partition row
-        VecT v0[kMergeChunk], v1[kMergeChunk];
-#pragma unroll
-        for (int qq = 0; qq < kMergeChunk; ++qq) {
-            if (qq < nparts) v0[qq] = __ldcg(src0 + qq * kStride);
-            if (qq < nparts && live1) v1[qq] = __ldcg(src1 + qq * kStride);
-        }
-        float wa[2], wb[2], inv[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float M = fmaxf(mla[j].y > 0.f ? mla[j].x : -INFINITY, mlb[j].y > 0.f ? mlb[j].x : -INFINITY);
-#pragma unroll
-            for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            wa[j] = (mla[j].y > 0.f && M != -INFINITY) ? fast_exp2(mla[j].x - M) : 0.f;
-            wb[j] = (mlb[j].y > 0.f && M != -INFINITY) ? fast_exp2(mlb[j].x - M) : 0.f;
-            float L = wa[j] * mla[j].y + wb[j] * mlb[j].y;
-#pragma unroll
-            for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-            inv[j] = L > 0.f ? 1.f / L : 0.f;
-        }
-        float acc0[kVec], acc1[kVec];
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) acc0[e] = acc1[e] = 0.f;
-        for (int q0 = 0; q0 < nparts; q0 += kMergeChunk) {
-            if (q0 > 0) {   // later chunks (more than kMergeChunk partitions)
-#pragma unroll
-                for (int qq = 0; qq < kMergeChunk; ++qq) {
-                    if (q0 + qq < nparts) v0[qq] = __ldcg(src0 + (q0 + qq) * kStride);
-                    if (q0 + qq < nparts && live1) v1[qq] = __ldcg(src1 + (q0 + qq) * kStride);
-                }
-            }
-#pragma unroll
-            for (int qq = 0; qq < kMergeChunk; ++qq) {
-                const int q = q0 + qq;
-                if (q < nparts) {   // warp-uniform
-                    const float w0 = __shfl_sync(0xffffffffu, q < 32 ? wa[0] : wb[0], q & 31);
-                    const float w1 = __shfl_sync(0xffffffffu, q < 32 ? wa[1] : wb[1], q & 31);
-#pragma unroll
-                    for (int e = 0; e < kVec; ++e) acc0[e] += w0 * vec_get(v0[qq], e);
-                    if (live1) {
-#pragma unroll
-                        for (int e = 0; e < kVec; ++e) acc1[e] += w1 * vec_get(v1[qq], e);
-                    }
-                }
-            }
-        }
-        const int64_t o0 = (static_cast<int64_t>(b) * p.num_heads + h0 + rg) * D + lane * kVec;
-#pragma unroll
-        for (int e = 0; e < kVec; e += 2) {
-            store_out2(p, o0 + e, acc0[e] * inv[0], acc0[e + 1] * inv[0]);
-            if (live1) store_out2(p, o0 + D + e, acc1[e] * inv[1], acc1[e + 1] * inv[1]);
+        if (v1) {
+            p.max_logits[row1] = st.l1 > 0.f ? st.t1 * kLn2 : -INFINITY;
+            p.exp_sums[row1] = st.l1 > 0.f ? st.l1 * fast_exp2(st.m1 - st.t1) : 0.f;
         }
     }
-    if (lane == 0) *counter = 0u;   // ready for the next call
 }
 
 // Split merged inside a thread-block cluster: the cluster is the nsplit
@@ -320,7 +197,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ DecodeParams p) {
     using C = MmaCfg<D, TT>;
-    constexpr int kNT = TT / 8;  // n-tiles of 8 tokens per tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -380,10 +256,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     __syncthreads();
 
     WarpState<D> st;
-    st.m0 = st.m1 = st.t0 = st.t1 = -INFINITY;
-    st.l0 = st.l1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+    st.init();
 
     if (warp == hpc) {
         // ------------------------------ producer ------------------------------
@@ -456,22 +329,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // ------------------------------ consumers -----------------------------
         const int gh = hgrp * hpc + warp;                     // this warp's KV head
         const int h0 = gh * p.group + tile * kRowsPerTile;    // its first query head
-        const int r = lane >> 2, q4 = lane & 3;
+        const int r = lane >> 2;
         uint32_t qa[D / 16][4];
         {
             const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
                 static_cast<const __nv_bfloat16 *>(p.query) +
                 (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D);
-            const uint32_t *q1 = q0 + 8 * (D / 2);
-            const bool v0 = r < rows, v1 = r + 8 < rows;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int c = (16 * kk + 2 * q4) / 2;
-                qa[kk][0] = v0 ? q0[c] : 0u;
-                qa[kk][1] = v1 ? q1[c] : 0u;
-                qa[kk][2] = v0 ? q0[c + 4] : 0u;
-                qa[kk][3] = v1 ? q1[c + 4] : 0u;
-            }
+            load_query_fragments<D>(qa, q0, q0 + 8 * (D / 2), r < rows, r + 8 < rows, lane);
         }
         const float sl2 = p.scale_log2;
 
@@ -498,103 +362,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 __syncwarp();
             }
 
-            // ---- S = Q K^T (two interleaved accumulator chains per n-tile) ----
-            float sacc[kNT][4];
-#pragma unroll
-            for (int j = 0; j < kNT; ++j) {
-                float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-                sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; kk += 2) {
-                    const int tok = 8 * j + (lane & 7);
-                    const int c = 2 * kk + (lane >> 3);
-                    const uint32_t addr = kbase + (c >> 3) * kHalfStride + tok_off(tok) +
-                                          (((c & 7) ^ (tok & 7)) << 4);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(addr, b0, b1, b2, b3);
-                    mma_bf16_16816(sacc[j], qa[kk], b0, b1);
-                    mma_bf16_16816(acc2, qa[kk + 1], b2, b3);
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sacc[j][e] = (sacc[j][e] + acc2[e]) * sl2;
-            }
-
-            // ---- online softmax (base 2) ----
-            if (valid < TT) {
-#pragma unroll
-                for (int j = 0; j < kNT; ++j)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        if (8 * j + 2 * q4 + e >= valid) sacc[j][e] = sacc[j][2 + e] = -INFINITY;
-            }
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < kNT; ++j) {
-                mx0 = fmaxf(mx0, fmaxf(sacc[j][0], sacc[j][1]));
-                mx1 = fmaxf(mx1, fmaxf(sacc[j][2], sacc[j][3]));
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            st.t0 = fmaxf(st.t0, mx0);
-            st.t1 = fmaxf(st.t1, mx1);
-            // Lazy rescale: the reference max only moves when a score exceeds it
-            // by more than kRescaleSlack (base 2), so 2^(s - m) stays <= 2^slack
-            // and the O rescale is skipped while no row in the warp needs it.
-            const bool need0 = mx0 > st.m0 + kRescaleSlack, need1 = mx1 > st.m1 + kRescaleSlack;
-            if (__any_sync(0xffffffffu, need0 || need1)) {
-                const float mn0 = need0 ? fmaxf(st.m0, mx0) : st.m0;
-                const float mn1 = need1 ? fmaxf(st.m1, mx1) : st.m1;
-                const float a0 = fast_exp2(st.m0 - mn0), a1 = fast_exp2(st.m1 - mn1);
-                st.m0 = mn0;
-                st.m1 = mn1;
-                st.l0 *= a0;
-                st.l1 *= a1;
-#pragma unroll
-                for (int i2 = 0; i2 < D / 8; ++i2) {
-                    st.o[i2][0] *= a0;
-                    st.o[i2][1] *= a0;
-                    st.o[i2][2] *= a1;
-                    st.o[i2][3] *= a1;
-                }
-            }
-            const float mn0 = st.m0, mn1 = st.m1;
-            uint32_t phi[4], plo[4];
-            phi[2] = phi[3] = plo[2] = plo[3] = 0u;
-#pragma unroll
-            for (int j = 0; j < kNT; ++j) {
-                const float p0 = fast_exp2(sacc[j][0] - mn0), p1 = fast_exp2(sacc[j][1] - mn0);
-                const float p2 = fast_exp2(sacc[j][2] - mn1), p3 = fast_exp2(sacc[j][3] - mn1);
-                st.l0 += p0 + p1;
-                st.l1 += p2 + p3;
-                split_bf16x2(p0, p1, phi[2 * j], plo[2 * j]);
-                split_bf16x2(p2, p3, phi[2 * j + 1], plo[2 * j + 1]);
-            }
-
-            // ---- O += P V ----
-#pragma unroll
-            for (int dn = 0; dn < D / 8; dn += 2) {
-                const int mi = lane >> 3;
-                const int tok = (mi & 1) * 8 + (lane & 7);
-                const int c = dn + (mi >> 1);
-                const uint32_t addr = vbase + (c >> 3) * kHalfStride + tok_off(tok) +
-                                      (((c & 7) ^ (tok & 7)) << 4);
-                uint32_t v0, v1, v2, v3;
-                ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-                mma_bf16_16816(st.o[dn], phi, v0, v1);
-                mma_bf16_16816(st.o[dn + 1], phi, v2, v3);
-                mma_bf16_16816(st.o[dn], plo, v0, v1);
-                mma_bf16_16816(st.o[dn + 1], plo, v2, v3);
-            }
+            warp_tile_attention<D, TT>(st, qa, kbase, vbase, kHalfStride, tok_off, valid, valid, sl2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[C::kMaxStages + s]));
         }
-        st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 1);
-        st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 2);
-        st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
-        st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
-        if (!cluster) warp_epilogue<D>(p, st, b, gh, tile, part, h0, rows, w.nparts, lane);
+        st.reduce_sums();
+        if (!cluster) warp_epilogue<D>(p, st, b, part, h0, rows, lane);
     }
 
     // Drain: wait (bounded) for the last phase of every stage this CTA armed,

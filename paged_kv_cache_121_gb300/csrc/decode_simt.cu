@@ -140,7 +140,7 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     }
     __syncthreads();
     combine_warps<D>(smem_f, kWarps, rows);
-    write_result<D>(p, smem_f, kWarps, b, g, tile, part, rows, w.nparts);
+    write_result<D>(p, smem_f, kWarps, b, g, tile, part, rows);
 }
 
 template <int D, int MAXR, typename KV>
@@ -186,7 +186,9 @@ lse_merge_kernel(void *out, int out_bf16, const float *tmp_out, const float *max
     const int h = blockIdx.x, b = blockIdx.y;
     int len = context_lens[b];
     if (len < 0) len = 0;
-    const int np = min((len + partition_size - 1) / partition_size, max_partitions);
+    // partition_size 0: every partition of the row (empty ones carry a zero sum)
+    const int np = partition_size > 0 ? min((len + partition_size - 1) / partition_size, max_partitions)
+                                      : max_partitions;
     const int64_t row0 = (static_cast<int64_t>(b) * num_heads + h) * max_partitions;
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
@@ -209,7 +211,7 @@ lse_merge_kernel(void *out, int out_bf16, const float *tmp_out, const float *max
     __syncthreads();
     const float inv = s_inv;
     for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
-        // partitions below np all hold tokens; independent loads, unrolled
+        // independent loads, unrolled (an empty partition holds zeros, weight 0)
         float acc = 0.f;
         const float *src = tmp_out + row0 * head_dim + d;
 #pragma unroll 8

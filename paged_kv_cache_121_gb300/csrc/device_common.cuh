@@ -12,12 +12,12 @@
 namespace pa {
 
 constexpr int kRowsPerTile = 16;     // query heads per CTA (the MMA's M)
-constexpr int kMaxSplits = 64;       // bound on fused partitions (the merge keeps two per lane)
+constexpr int kMaxSplits = 64;       // most partitions pa_decode's plan cuts one context into
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far above any legal wait
 
-enum DecodeMode : int { kModeFinal = 0, kModeSplitK = 1, kModeFused = 2 };
+enum DecodeMode : int { kModeFinal = 0, kModeSplitK = 1 };
 enum StatusCode : int { kStatusTimeout = 5 };
 
 // Everything a decode launch needs; passed by value.
@@ -31,9 +31,6 @@ struct DecodeParams {
     float *tmp_out;      // split-K mode
     float *max_logits;
     float *exp_sums;
-    float *ws_o;         // fused mode: [B, Hq, nsplit, D] unnormalised partials
-    float *ws_ml;        // fused mode: [B, Hq, nsplit, 2] (max in log2 units, sum)
-    unsigned *ws_count;  // fused mode: [B, Hkv, ntile] arrival counters (zero between calls)
     int *status;         // device status word
     int num_seqs, num_heads, num_kv_heads, head_dim, block_size;
     int max_blocks, num_blocks;
@@ -47,10 +44,32 @@ struct DecodeParams {
                          // (grid.x = nsplit = cluster size)
     int nsplit;          // grid.x: partitions per (sequence, head tile)
     int part_tokens;     // tokens per partition (a multiple of the kernel's tile length)
+    int skip_tokens;     // each context's first skip_tokens tokens are not attended here
+                         // (a shared prefix attended by the prefix pass)
+    int part_stride;     // split-K rows: partitions per (sequence, head) in tmp_out (0: nsplit)
+    int part_offset;     //   and the index of this launch's partition 0 there
     int mode;
     int out_bf16;
     int q_bf16;
     float scale_log2;    // scale * log2(e): scores are kept in base-2 units
+};
+
+// Shared-prefix pass: attention of every (sequence, query head) row over the
+// shared leading blocks, one chunk per partition, in split-K form.
+struct PrefixParams {
+    const void *query;            // [B, Hq, D] bf16
+    const int32_t *prefix_table;  // the shared leading block ids (a block-table row)
+    const int32_t *context_lens;  // [B]
+    float *tmp_out;               // [B, Hq, part_stride, D]: chunk c at partition c
+    float *max_logits;            // [B, Hq, part_stride]
+    float *exp_sums;              // [B, Hq, part_stride]
+    int *status;                  // device status word
+    int num_seqs, num_heads, num_kv_heads, head_dim, group, block_size;
+    int prefix_tokens;            // tokens in the shared blocks attended here (a multiple of 16)
+    int chunk_tokens;             // tokens per chunk (a multiple of 16)
+    int part_stride;              // partitions per row in tmp_out
+    int ring_bytes;
+    float scale_log2;
 };
 
 // Raise a kernel's dynamic shared-memory limit once per device (host side;
@@ -219,6 +238,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // ---------------------------------------------------------------------------
 // warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate)
 // ---------------------------------------------------------------------------
@@ -245,12 +270,19 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Split-K row of (sequence b, query head h, partition part) in tmp_out /
+// max_logits / exp_sums.
+__device__ __forceinline__ int64_t split_row(const DecodeParams &p, int b, int h, int part) {
+    const int stride = p.part_stride > 0 ? p.part_stride : p.nsplit;
+    return (static_cast<int64_t>(b) * p.num_heads + h) * stride + p.part_offset + part;
+}
+
 // ---------------------------------------------------------------------------
 // Per-sequence bookkeeping shared by every decode kernel
 // ---------------------------------------------------------------------------
 struct SeqWork {
     int len;        // tokens attended (clamped to the cache's capacity and the grid's reach)
-    int nparts;     // partitions with work (fused / final modes)
+    int nparts;     // partitions with work
     int tok_begin;  // this CTA's first token
     int tok_end;    // one past its last token (<= tok_begin: nothing to do)
 };
@@ -261,11 +293,12 @@ __device__ __forceinline__ SeqWork seq_work(const DecodeParams &p, int b, int pa
     if (len < 0) len = 0;
     const int cap = p.contig_stride > 0 ? p.contig_stride : p.max_blocks * p.block_size;
     if (len > cap) len = cap;
-    const int64_t reach = static_cast<int64_t>(p.nsplit) * p.part_tokens;
+    const int first = min(p.skip_tokens, len);
+    const int64_t reach = first + static_cast<int64_t>(p.nsplit) * p.part_tokens;
     if (len > reach) len = static_cast<int>(reach);
     w.len = len;
-    w.nparts = (len + p.part_tokens - 1) / p.part_tokens;
-    w.tok_begin = part * p.part_tokens;
+    w.nparts = (len - first + p.part_tokens - 1) / p.part_tokens;
+    w.tok_begin = first + part * p.part_tokens;
     w.tok_end = min(len, w.tok_begin + p.part_tokens);
     return w;
 }
@@ -276,7 +309,6 @@ __device__ __forceinline__ SeqWork seq_work(const DecodeParams &p, int b, int pa
 // Shared-memory layout (floats), row stride D + 4:
 //   warp region w: m[16], l[16], O[16][D+4]   for w < nwarps
 //   cta region:    m[16], l[16], O[16][D+4]
-//   merge weights: [16][kMaxSplits]
 // m is a running max of base-2 scores, l the sum of 2^(s - m), O the
 // unnormalised sum of 2^(s - m) * v.
 // ---------------------------------------------------------------------------
@@ -288,8 +320,7 @@ struct MergeLayout {
     __device__ static float *l(float *base, int w) { return base + w * kRegion + 16; }
     __device__ static float *o(float *base, int w) { return base + w * kRegion + 32; }
     static constexpr size_t bytes(int nwarps) {
-        return sizeof(float) * (static_cast<size_t>(nwarps + 1) * kRegion +
-                                static_cast<size_t>(kRowsPerTile) * kMaxSplits);
+        return sizeof(float) * static_cast<size_t>(nwarps + 1) * kRegion;
     }
 };
 
@@ -331,13 +362,11 @@ __device__ __forceinline__ void store_out(const DecodeParams &p, int64_t idx, fl
 // Write rows [0, rows) of the CTA result for (b, kv head g, head tile, partition).
 template <int D>
 __device__ void write_result(const DecodeParams &p, float *base, int nwarps, int b, int g,
-                             int tile, int part, int rows, int nparts) {
+                             int tile, int part, int rows) {
     using L = MergeLayout<D>;
     float *cm = L::m(base, nwarps), *cl = L::l(base, nwarps), *co = L::o(base, nwarps);
     const int h0 = g * p.group + tile * kRowsPerTile;
-    const int mode = (p.mode == kModeFused && nparts <= 1) ? kModeFinal : p.mode;
-
-    if (mode == kModeFinal) {
+    if (p.mode == kModeFinal) {
         for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
             const int r = idx / D, d = idx % D;
             const float l = cl[r];
@@ -346,80 +375,20 @@ __device__ void write_result(const DecodeParams &p, float *base, int nwarps, int
         }
         return;
     }
-    if (mode == kModeSplitK) {
-        const int P = p.nsplit;
-        for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
-            const int r = idx / D, d = idx % D;
-            const float l = cl[r];
-            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * P + part;
-            p.tmp_out[row * D + d] = l > 0.f ? co[r * L::kStride + d] / l : 0.f;
-        }
-        if (threadIdx.x < rows) {
-            const int r = threadIdx.x;
-            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * P + part;
-            const float l = cl[r];
-            p.max_logits[row] = l > 0.f ? cm[r] * kLn2 : -INFINITY;
-            p.exp_sums[row] = l;
-        }
-        return;
-    }
-
-    // fused: publish this partition, the last CTA to arrive merges them all
-    const int S = p.nsplit;
+    // split-K: normalised partial output, its maximum (natural log units) and sum
     for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
         const int r = idx / D, d = idx % D;
-        const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S + part;
-        p.ws_o[row * D + d] = co[r * L::kStride + d];
+        const float l = cl[r];
+        const int64_t row = split_row(p, b, h0 + r, part);
+        p.tmp_out[row * D + d] = l > 0.f ? co[r * L::kStride + d] / l : 0.f;
     }
     if (threadIdx.x < rows) {
         const int r = threadIdx.x;
-        const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S + part;
-        p.ws_ml[row * 2 + 0] = cm[r];
-        p.ws_ml[row * 2 + 1] = cl[r];
+        const int64_t row = split_row(p, b, h0 + r, part);
+        const float l = cl[r];
+        p.max_logits[row] = l > 0.f ? cm[r] * kLn2 : -INFINITY;
+        p.exp_sums[row] = l;
     }
-    __threadfence();
-    __syncthreads();
-    __shared__ unsigned s_last;
-    unsigned *counter = p.ws_count + (static_cast<int64_t>(b) * p.num_kv_heads + g) * p.ntile + tile;
-    if (threadIdx.x == 0) {
-        const unsigned prev = atomicAdd(counter, 1u);
-        s_last = (prev == static_cast<unsigned>(nparts - 1)) ? 1u : 0u;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-
-    float *wgt = base + (nwarps + 1) * L::kRegion;  // [16][kMaxSplits]
-    __shared__ float s_inv[kRowsPerTile];
-    if (threadIdx.x < rows) {
-        const int r = threadIdx.x;
-        const int64_t row0 = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S;
-        float M = -INFINITY;
-        for (int q = 0; q < nparts; ++q) {
-            const float l = __ldcg(p.ws_ml + (row0 + q) * 2 + 1);
-            if (l > 0.f) M = fmaxf(M, __ldcg(p.ws_ml + (row0 + q) * 2 + 0));
-        }
-        float tot = 0.f;
-        for (int q = 0; q < nparts; ++q) {
-            const float l = __ldcg(p.ws_ml + (row0 + q) * 2 + 1);
-            const float w = l > 0.f ? fast_exp2(__ldcg(p.ws_ml + (row0 + q) * 2 + 0) - M) : 0.f;
-            wgt[r * kMaxSplits + q] = w;
-            tot += w * l;
-        }
-        s_inv[r] = tot > 0.f ? 1.f / tot : 0.f;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
-        const int r = idx / D, d = idx % D;
-        const int64_t row0 = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * S;
-        float acc = 0.f;
-        for (int q = 0; q < nparts; ++q) {
-            const float w = wgt[r * kMaxSplits + q];
-            if (w != 0.f) acc += w * __ldcg(p.ws_o + (row0 + q) * D + d);
-        }
-        store_out(p, (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + d, acc * s_inv[r]);
-    }
-    if (threadIdx.x == 0) *counter = 0u;  // ready for the next call
 }
 
 // One warp, one KV head: rows h0 .. h0+rows-1 of a partition holding no tokens.
@@ -427,9 +396,8 @@ template <int D>
 __device__ void warp_write_empty(const DecodeParams &p, int b, int h0, int part, int rows, int nparts,
                                  int lane) {
     if (p.mode == kModeSplitK) {
-        const int P = p.nsplit;
         for (int r = 0; r < rows; ++r) {
-            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * P + part;
+            const int64_t row = split_row(p, b, h0 + r, part);
             for (int d = lane; d < D; d += 32) p.tmp_out[row * D + d] = 0.f;
             if (lane == 0) {
                 p.max_logits[row] = -INFINITY;
@@ -450,20 +418,19 @@ __device__ void write_empty(const DecodeParams &p, int b, int g, int tile, int p
                             int nparts) {
     const int h0 = g * p.group + tile * kRowsPerTile;
     if (p.mode == kModeSplitK) {
-        const int P = p.nsplit;
         for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
             const int r = idx / D, d = idx % D;
-            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * P + part;
+            const int64_t row = split_row(p, b, h0 + r, part);
             p.tmp_out[row * D + d] = 0.f;
         }
         if (threadIdx.x < rows) {
-            const int64_t row = (static_cast<int64_t>(b) * p.num_heads + h0 + threadIdx.x) * P + part;
+            const int64_t row = split_row(p, b, h0 + threadIdx.x, part);
             p.max_logits[row] = -INFINITY;
             p.exp_sums[row] = 0.f;
         }
         return;
     }
-    // final / fused: an empty sequence has one all-zero output row, written by partition 0
+    // final: an empty sequence has one all-zero output row, written by partition 0
     if (nparts == 0 && part == 0)
         for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
             const int r = idx / D, d = idx % D;

@@ -8,6 +8,7 @@
 namespace pa {
 
 struct DecodeParams;
+struct PrefixParams;
 
 bool decode_mma_supported(int head_dim, int block_size);
 int decode_mma_tile_tokens(int block_size);       // tokens per pipeline stage (16)
@@ -18,6 +19,12 @@ int decode_mma_cluster_bytes(int head_dim, int heads_per_cta);   // shared memor
 constexpr int kMaxClusterSplits = 8;                              // portable cluster size
 cudaError_t launch_decode_mma(const DecodeParams &p, const CUtensorMap &tmap_k,
                               const CUtensorMap &tmap_v, dim3 grid, cudaStream_t stream);
+// Shared-prefix pass (prefix_mma.cu): grid (chunks, Hkv, row groups).
+constexpr int kPrefixMaxRingBytes = 128 * 1024;
+int prefix_rows_per_cta();
+int prefix_stage_bytes(int head_dim);
+cudaError_t launch_prefix_mma(const PrefixParams &p, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                              dim3 grid, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
                              const float *exp_sums, const int32_t *context_lens, int num_seqs,

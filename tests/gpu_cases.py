@@ -33,8 +33,8 @@ class DeviceBatch:
         self.v_cache = to_dev(batch.v_cache)
         self.block_tables = to_dev(batch.block_tables)
         self.context_lens = to_dev(batch.context_lens)
-        self.new_key = to_dev(batch.new_key)
-        self.new_value = to_dev(batch.new_value)
+        self.new_key = to_dev(batch.new_key) if batch.new_key is not None else None
+        self.new_value = to_dev(batch.new_value) if batch.new_value is not None else None
 
 
 def new_token_slots(batch) -> np.ndarray:

@@ -173,6 +173,43 @@ def make_batch(name: str, context_lens, num_heads: int, num_kv_heads: int, head_
                        head_dim=head_dim, scale=1.0 / math.sqrt(head_dim), bf16=bf16)
 
 
+def shared_prefix_batch(name: str, shared_blocks: int, suffix_lens, num_heads: int, num_kv_heads: int,
+                        head_dim: int, block_size: int, spare_blocks: int = 7,
+                        seed_values: int = SEED_VALUES, seed_blocks: int = SEED_BLOCKS) -> DecodeBatch:
+    """A bf16 decode batch whose sequences share their first ``shared_blocks``
+    (full) blocks: every table row starts with the same physical ids, then
+    each sequence's private blocks for ``suffix_lens[b]`` more tokens. Ids
+    are a seeded permutation of a pool with ``spare_blocks`` unused blocks."""
+    suffix = np.asarray(suffix_lens, dtype=np.int64)
+    B = suffix.size
+    lens = (shared_blocks * block_size + suffix).astype(np.int32)
+    need_priv = [cdiv(int(n), block_size) - shared_blocks for n in lens]
+    num_blocks = shared_blocks + sum(need_priv) + spare_blocks
+    max_blocks = max(1, max(cdiv(int(n), block_size) for n in lens))
+    perm = np.random.default_rng(seed_blocks).permutation(num_blocks).astype(np.int32)
+    tables = np.zeros((B, max_blocks), dtype=np.int32)
+    tables[:, :shared_blocks] = perm[:shared_blocks]
+    pos = shared_blocks
+    for b, n in enumerate(need_priv):
+        tables[b, shared_blocks:shared_blocks + n] = perm[pos:pos + n]
+        pos += n
+    rng = np.random.default_rng(seed_values)
+    shape = (num_blocks, block_size, num_kv_heads, head_dim)
+    k_cache = np.zeros(shape, dtype=np.uint16)
+    v_cache = np.zeros(shape, dtype=np.uint16)
+    used = perm[:pos]
+    k_cache[used] = _normal(rng, (used.size,) + shape[1:], True)
+    v_cache[used] = _normal(rng, (used.size,) + shape[1:], True)
+    query = _normal(rng, (B, num_heads, head_dim), True)
+    new_key = _normal(rng, (B, num_kv_heads, head_dim), True)
+    new_value = _normal(rng, (B, num_kv_heads, head_dim), True)
+    return DecodeBatch(name=name, query=query, k_cache=k_cache, v_cache=v_cache, block_tables=tables,
+                       context_lens=lens, new_key=new_key, new_value=new_value,
+                       new_pos=np.maximum(lens - 1, 0).astype(np.int32), block_size=block_size,
+                       num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                       scale=1.0 / math.sqrt(head_dim), bf16=True)
+
+
 # --------------------------------------------------------------------------
 # The five workloads
 # --------------------------------------------------------------------------

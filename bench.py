@@ -238,14 +238,24 @@ def cpu_baseline(batch, nseq_batch, budget_s=10.0):
         if reps >= 1000:
             break
     kvb = kv_bytes(lens, batch.num_kv_heads, batch.head_dim, batch.elem_bytes) * reps
+    # the same oracle on one thread, over a smaller sample (a quarter of the batch, twice)
+    one = seqs[: max(1, nseq_batch // 4)]
+    t1 = sum(oracle_units_time(batch, one, 1) for _ in range(2))
+    kv1 = kv_bytes(batch.context_lens[one], batch.num_kv_heads, batch.head_dim, batch.elem_bytes) * 2
     return {"value": kvb / elapsed / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": f"{reps} full decode step(s) of the workload ({nseq_batch} sequences, fp64 C, "
                       f"OpenMP over (sequence, KV head)), {elapsed:.1f} s",
-            "tokens_per_s": nseq_batch * reps / elapsed}
+            "tokens_per_s": nseq_batch * reps / elapsed,
+            "single_thread": {"value": kv1 / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{len(one)} sequence(s) x 2, {t1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
+        return 0
+    if args.config == "cow":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the paged workloads "
+                          "(qwen3, long, gqa); the copy-on-write state is built by the library"}), flush=True)
         return 0
     batch, desc = build_workload(args.config, 0, 1, args.block_size)
     nb = per_batch(args.config)
@@ -440,6 +450,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
     torch.cuda.synchronize()
     decode_ms = e0.elapsed_time(e1) / (dreps * GRAPH_STEPS)
+    scatter_ms, _ = time_graph(torch, stream, lambda i: scatter(views[i % copies]), dreps)
 
     # e2e through the public API, host buffers (pinned), copies inside the timed region
     h_in = []
@@ -544,6 +555,10 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms_step, "steps": e2e_steps},
         "gpu_launches": (1 + decode_launches) * steps_timed,
+        "components": {"reshape_and_cache_us": scatter_ms * 1e3,
+                       "reshape_and_cache_gbs": nb * hkv * d * elem * 2 * 2 / (scatter_ms * 1e-3) / 1e9,
+                       "reshape_and_cache_tokens": nb},
+        "tokens_per_s_36_layers_attention_only": world * nb / (36 * ms_step * 1e-3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not contig:
         line["cpu_baseline"] = cpu_baseline(batch, nb, budget_s=args.cpu_seconds)
@@ -554,13 +569,285 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# copy-on-write workload: 64 sequences forked from one prefix
+# ---------------------------------------------------------------------------
+COW_COPIES = 6      # disjoint copies of the workload (6 x ~42 MB unique > L2)
+
+
+def build_cow_state(torch, pa, copies: int, prefix_len: int):
+    """The copy-on-write workload built through the library: per copy, one
+    sequence is prefilled with the shared prefix, forked to 63 more, every
+    sequence appends its suffix through the block manager (copy-on-write of
+    the half-filled shared block by copy_blocks), and the decode token's slot
+    is allocated. Returns the device caches and, per copy, the step's inputs."""
+    case = workloads.shared_prefix(prefix_len=prefix_len)
+    S, bs, hkv, d = len(case.suffix_lens), case.block_size, case.num_kv_heads, case.head_dim
+    nblocks = case.num_blocks * copies
+    k_cache = torch.zeros((nblocks, bs, hkv, d), dtype=torch.bfloat16, device="cuda")
+    v_cache = torch.zeros_like(k_cache)
+    bm = pa.BlockManager(nblocks, bs)
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    views, pairs_all = [], []
+    for c in range(copies):
+        base = c * S
+        bm.allocate(base, prefix_len)
+        slots = pa.pa_compute_slot_mapping(np.array([bm.block_table(base)], np.int32),
+                                           np.zeros(prefix_len, np.int32), np.arange(prefix_len, dtype=np.int32), bs)
+        pa.pa_reshape_and_cache(dev(case.prefix_key), dev(case.prefix_value), k_cache, v_cache,
+                                torch.from_numpy(slots).cuda())
+        for s_ in range(1, S):
+            bm.fork(base, base + s_)
+        pairs, slots, keys, vals, dec_slots = [], [], [], [], []
+        for s_ in range(S):
+            n = case.suffix_key[s_].shape[0]
+            for t in range(n):
+                slot, src, dst = bm.append_slot(base + s_)
+                if src >= 0:
+                    pairs.append((src, dst))
+                if t < n - 1:
+                    slots.append(slot)
+                else:
+                    dec_slots.append(slot)      # the decode token: written inside the timed step
+            keys.append(case.suffix_key[s_][:-1])
+            vals.append(case.suffix_value[s_][:-1])
+        if pairs:
+            pa.pa_copy_blocks(k_cache, v_cache, torch.from_numpy(np.array(pairs, np.int64)).cuda())
+        if slots:
+            pa.pa_reshape_and_cache(dev(np.concatenate(keys)), dev(np.concatenate(vals)), k_cache, v_cache,
+                                    torch.from_numpy(np.array(slots, np.int64)).cuda())
+        lens = np.array([bm.num_tokens(base + s_) for s_ in range(S)], np.int32)
+        maxb = max(len(bm.block_table(base + s_)) for s_ in range(S))
+        tables = np.zeros((S, maxb), np.int32)
+        for s_ in range(S):
+            t = bm.block_table(base + s_)
+            tables[s_, :len(t)] = t
+        dk = np.stack([case.suffix_key[s_][-1] for s_ in range(S)])
+        dv = np.stack([case.suffix_value[s_][-1] for s_ in range(S)])
+        views.append({"query": dev(case.query), "tables": torch.from_numpy(tables).cuda(),
+                      "lens": torch.from_numpy(lens).cuda(), "lens_h": lens, "key": dev(dk), "value": dev(dv),
+                      "slots": torch.from_numpy(np.array(dec_slots, np.int64)).cuda(),
+                      "max_len": int(lens.max()), "shared": prefix_len // bs,
+                      "out": torch.empty((S, case.num_heads, d), dtype=torch.float32, device="cuda"),
+                      "host": {"query": case.query, "tables": tables, "lens": lens, "key": dk, "value": dv,
+                               "slots": np.array(dec_slots, np.int64)}})
+        pairs_all.append(np.array(pairs, np.int64).reshape(-1, 2))
+    torch.cuda.synchronize()
+    return case, k_cache, v_cache, views, pairs_all, bm.stats()
+
+
+def time_graph(torch, stream, fn, reps: int):
+    """Device time of one call of fn: a CUDA graph of GRAPH_STEPS calls
+    replayed reps times, CUDA events on the graph's stream."""
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for i in range(GRAPH_STEPS):
+            fn(i)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * GRAPH_STEPS), g
+
+
+def run_cow(args, rank, world, local_rank):
+    """Copy-on-write workload (64 sequences sharing a 2,064-token prefix in
+    blocks of 32, suffixes U[0, 256]): a step scatters each sequence's decode
+    token and runs one decode, plain (pa_decode: every sequence reads the
+    prefix through its own table) or prefix-aware (pa_decode_shared_prefix:
+    the 64 shared blocks read once)."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_121_gb300 as pa
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    pa.load_library()
+    prefix_len = 2064
+    copies = args.copies or COW_COPIES
+    case, k_cache, v_cache, views, pairs_all, stats = build_cow_state(torch, pa, copies, prefix_len)
+    S, hq, hkv, d, bs = len(case.suffix_lens), case.num_heads, case.num_kv_heads, case.head_dim, case.block_size
+    shared = prefix_len // bs
+    aware = args.prefix_aware
+    mcl = max(v["max_len"] for v in views)
+    if aware:
+        ws_bytes = pa.pa_decode_shared_prefix_workspace_size(S, hq, hkv, d, bs, mcl, shared)
+    else:
+        ws_bytes = pa.pa_decode_workspace_size(S, hq, hkv, d, bs, mcl)
+    workspace = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+
+    def decode_into(out, v, query, lens, tables):
+        if aware:
+            pa.pa_decode_shared_prefix(out, query, k_cache, v_cache, tables, lens, v["max_len"], v["shared"],
+                                       case.scale, workspace)
+        else:
+            pa.pa_decode(out, query, k_cache, v_cache, tables, lens, v["max_len"], case.scale,
+                         workspace=workspace)
+
+    def step(i):
+        v = views[i % copies]
+        pa.pa_reshape_and_cache(v["key"], v["value"], k_cache, v_cache, v["slots"])
+        decode_into(v["out"], v, v["query"], v["lens"], v["tables"])
+
+    def decode(i):
+        v = views[i % copies]
+        decode_into(v["out"], v, v["query"], v["lens"], v["tables"])
+
+    # copy_blocks of one copy's copy-on-write pairs, into spare blocks (the
+    # same bytes as the real copies, without undoing the suffixes written since)
+    npairs = int(pairs_all[0].shape[0])
+    scratch_pairs = pairs_all[0].copy()
+    scratch_pairs[:, 1] = np.arange(k_cache.shape[0] - npairs, k_cache.shape[0])
+    scratch_pairs_d = torch.from_numpy(scratch_pairs).cuda()
+
+    stream = torch.cuda.Stream()
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+    torch.cuda.synchronize()
+    if pa.pa_device_status() != 0:
+        raise SystemExit("device status not clean after warm-up")
+    if args.profile_steps:
+        for i in range(args.profile_steps):
+            step(i)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_steps": args.profile_steps, "config": "cow", "prefix_aware": aware}), flush=True)
+        return 0
+    reps = max(5, K // GRAPH_STEPS)
+    sampler = ClockSampler(gpu_id_for_smi(torch, local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    t_wall0 = time.perf_counter()
+    step_ms, _ = time_graph(torch, stream, step, reps)
+    t_wall1 = time.perf_counter()
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
+    decode_ms, _ = time_graph(torch, stream, decode, reps)
+    scatter_ms, _ = time_graph(torch, stream, lambda i: pa.pa_reshape_and_cache(
+        views[i % copies]["key"], views[i % copies]["value"], k_cache, v_cache, views[i % copies]["slots"]), reps)
+    copy_ms, _ = time_graph(torch, stream, lambda i: pa.pa_copy_blocks(k_cache, v_cache, scratch_pairs_d), reps)
+    if pa.pa_device_status() != 0:
+        raise SystemExit("device status not clean after the timed region")
+
+    # e2e through the public API: host inputs in, output out, every step
+    h_in = []
+    for v in views:
+        h = v["host"]
+        h_in.append({k: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else
+                                         np.ascontiguousarray(a)).pin_memory() for k, a in h.items()})
+        h_in[-1]["out"] = torch.empty((S, hq, d), dtype=torch.float32).pin_memory()
+    dq = torch.empty((S, hq, d), dtype=torch.bfloat16, device="cuda")
+    dk = torch.empty((S, hkv, d), dtype=torch.bfloat16, device="cuda")
+    dvv = torch.empty_like(dk)
+    dl = torch.empty((S,), dtype=torch.int32, device="cuda")
+    ds = torch.empty((S,), dtype=torch.int64, device="cuda")
+    dts = [torch.empty_like(v["tables"]) for v in views]
+    dout = torch.empty((S, hq, d), dtype=torch.float32, device="cuda")
+
+    def e2e_step(i):
+        h, v, dt = h_in[i % copies], views[i % copies], dts[i % copies]
+        dq.view(torch.int16).copy_(h["query"], non_blocking=True)
+        dk.view(torch.int16).copy_(h["key"], non_blocking=True)
+        dvv.view(torch.int16).copy_(h["value"], non_blocking=True)
+        dt.copy_(h["tables"], non_blocking=True)
+        dl.copy_(h["lens"], non_blocking=True)
+        ds.copy_(h["slots"], non_blocking=True)
+        pa.pa_reshape_and_cache(dk, dvv, k_cache, v_cache, ds)
+        decode_into(dout, v, dq, dl, dt)
+        h["out"].copy_(dout, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return float(h["out"][0, 0, 0])
+
+    for i in range(3):
+        e2e_step(i)
+    e2e_steps = min(K, 2000)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    h2d = sum(h_in[0][k].numel() * h_in[0][k].element_size() for k in ("query", "tables", "lens", "key", "value", "slots"))
+    d2h = S * hq * d * 4
+    if world > 1:
+        step_ms, decode_ms, e2e_ms = max_over_ranks([step_ms, decode_ms, e2e_ms], "cuda")
+
+    lens0 = views[0]["lens_h"]
+    logical = kv_bytes(lens0, hkv, d, 2)                                  # every sequence's whole context
+    private_blocks = sum(workloads.cdiv(int(n), bs) - shared for n in lens0)
+    unique = (shared + private_blocks) * bs * hkv * d * 2 * 2              # each block once
+    alg = unique + S * hq * d * 2 + S * hq * d * 4 + tables_bytes(lens0, bs) + S * 4
+    peak, peak_kind = measured_peaks()
+    value = whole_job_gbs(world, logical, step_ms)
+    line = {
+        "metric": "decode attention KV GB/s, copy-on-write shared-prefix workload (logical bytes)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": reps * GRAPH_STEPS, "warmup": W,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), bf16-rounded; blocks placed by the block manager)",
+        "config": {"workload": "cow: 64 seqs sharing a %d-token prefix, suffix U[0,256] + 1 decode token, "
+                               "Hq 32, Hkv 8, D 128, bf16, block 32" % prefix_len,
+                   "decode": "pa_decode_shared_prefix (%d shared blocks read once)" % shared if aware
+                   else "pa_decode (each sequence reads the prefix through its table)",
+                   "graphs": "%d steps per CUDA graph, %d copies of the workload alternate" % (GRAPH_STEPS, copies),
+                   "l2": "inputs larger than L2: %d copies x %.0f MB unique" % (copies, unique / 1e6),
+                   "cow_pairs_per_copy": npairs},
+        "unique_kv_gbs": whole_job_gbs(world, unique, step_ms),
+        "tokens_per_s": world * S / (step_ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": alg / (decode_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": alg / (decode_ms * 1e-3) / 1e9 / peak, "traffic": None,
+                     "kernel": "prefix pass + decode + merge" if aware else "decode_mma_kernel<128,16>",
+                     "peak_kind": peak_kind, "decode_us": decode_ms * 1e3, "alg_bytes_per_launch": int(alg),
+                     "alg_bytes": "unique K/V bytes (each block once) + q + out + table + lengths"},
+        "components": {
+            "reshape_and_cache_us": scatter_ms * 1e3,
+            "reshape_and_cache_gbs": S * hkv * d * 2 * 2 * 2 / (scatter_ms * 1e-3) / 1e9,
+            "copy_blocks_us": copy_ms * 1e3,
+            "copy_blocks_pairs": npairs,
+            "copy_blocks_gbs": npairs * bs * hkv * d * 2 * 2 * 2 / (copy_ms * 1e-3) / 1e9,
+        },
+        "clocks": clocks,
+        "e2e": {"value": whole_job_gbs(world, logical, e2e_ms), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": (1 + (3 if aware else pa.pa_decode_plan(S, hq, hkv, d, bs, mcl)["kernel_launches"]))
+                        * reps * GRAPH_STEPS,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def tables_bytes(lens, bs) -> int:
+    return sum(workloads.cdiv(int(n), bs) for n in lens) * 4
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["qwen3", "long", "gqa"], default="qwen3")
+    ap.add_argument("--config", choices=["qwen3", "long", "gqa", "cow"], default="qwen3")
+    ap.add_argument("--copies", type=int, default=0,
+                    help="cow: disjoint copies of the workload held on the device (default %d)" % COW_COPIES)
+    ap.add_argument("--prefix-aware", action="store_true",
+                    help="cow: decode with pa_decode_shared_prefix (the shared blocks read once)")
     ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
                     help="contiguous: the same lengths in one reservation per sequence, no block table")
     ap.add_argument("--block-size", type=int, default=16, choices=[4, 8, 16, 32, 64, 128],
@@ -577,6 +864,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.config == "cow":
+        return run_cow(args, rank, world, local_rank)
     return run_ours(args, rank, world, local_rank)
 
 

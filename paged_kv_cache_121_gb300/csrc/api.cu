@@ -405,7 +405,7 @@ PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms) {
     rest.max_ctx = static_cast<int>(std::max<int64_t>(0, s.max_ctx - P));
     pp.suffix = plan_split(rest, sms, true);
     pp.suffix.cluster = false;
-    pp.part_stride = pp.chunks + pp.suffix.nsplit;
+    pp.part_stride = pp.chunks + pp.suffix.nsplit;   // the rest's partitions follow the prefix chunks
     return pp;
 }
 
@@ -669,7 +669,7 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
                         static_cast<unsigned>(pp.row_groups));
         if (launch_prefix_mma(pq, tk, tv, grid, strm) != cudaSuccess) return PA_ERR_CUDA;
     }
-    // 2. the rest of every context, split-K partitions after the prefix chunks
+    // 2. the rest of every context (the tokens past the shared ones)
     DecodeParams p;
     fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
     p.tmp_out = tmp_out;
@@ -681,6 +681,7 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     p.part_tokens = pp.suffix.part_tokens;
     p.skip_tokens = pp.prefix_tokens;
     p.part_stride = pp.part_stride;
+    // split-K partitions after the prefix chunks, then the merge
     p.part_offset = pp.chunks;
     p.mode = kModeSplitK;
     if ((st = launch_decode(s, p, kv_dtype, true, dev, strm)) != PA_OK) return st;

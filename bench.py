@@ -253,9 +253,9 @@ def cpu_baseline(batch, nseq_batch, budget_s=10.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    if args.config == "cow":
-        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the paged workloads "
-                          "(qwen3, long, gqa); the copy-on-write state is built by the library"}), flush=True)
+    if args.config in ("cow", "swap"):
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the paged decode "
+                          "workloads (qwen3, long, gqa)"}), flush=True)
         return 0
     batch, desc = build_workload(args.config, 0, 1, args.block_size)
     nb = per_batch(args.config)
@@ -833,6 +833,112 @@ def run_cow(args, rank, world, local_rank):
     return 0
 
 
+def run_swap(args, rank, world, local_rank):
+    """Swap of the Qwen3-8B layer's KV (16 sequences x 4,164 tokens, 261
+    blocks of 16 each) to a page-locked CPU pool and back: one pa_swap_blocks
+    launch per direction, against one copy call per block and cache (the
+    many small transfers the pages describe), captured in a CUDA graph."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_121_gb300 as pa
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    pa.load_library()
+    batch = workloads.qwen3(num_seqs=16, copies=1)
+    hkv, d, bs = batch.num_kv_heads, batch.head_dim, batch.block_size
+    kd = torch.from_numpy(batch.k_cache.view(np.int16)).cuda().view(torch.bfloat16)
+    vd = torch.from_numpy(batch.v_cache.view(np.int16)).cuda().view(torch.bfloat16)
+    used = [batch.block_tables[i, :workloads.cdiv(int(n), bs)] for i, n in enumerate(batch.context_lens)]
+    nblk = int(sum(len(u) for u in used))
+    # the batch's placement: device block -> CPU block pairs, CPU ids 0..nblk-1
+    out_pairs = np.stack([np.concatenate(used).astype(np.int64), np.arange(nblk, dtype=np.int64)], 1)
+    in_pairs = out_pairs[:, ::-1].copy()
+    hk = torch.empty((nblk, bs, hkv, d), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    po, pi = torch.from_numpy(out_pairs).cuda(), torch.from_numpy(in_pairs).cuda()
+    moved = nblk * bs * hkv * d * 2 * 2                       # K and V bytes, one direction
+    stream = torch.cuda.Stream()
+    reps = max(3, args.steps // GRAPH_STEPS)
+
+    def kernel_step(i):
+        pa.pa_swap_blocks(hk, hv, kd, vd, po)
+        pa.pa_swap_blocks(kd, vd, hk, hv, pi)
+
+    def per_block_step(i):
+        for g, h in out_pairs[:, :2].tolist():
+            hk[h].copy_(kd[g], non_blocking=True)
+            hv[h].copy_(vd[g], non_blocking=True)
+        for g, h in out_pairs[:, :2].tolist():
+            kd[g].copy_(hk[h], non_blocking=True)
+            vd[g].copy_(hv[h], non_blocking=True)
+
+    sampler = ClockSampler(gpu_id_for_smi(torch, local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    k_ms, _ = time_graph(torch, stream, kernel_step, reps)
+    t1 = time.perf_counter()
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(t0 - 0.05, t1 + 0.05)
+    b_ms = time_graph_once(torch, stream, per_block_step, max(3, reps // 20))
+    # the link's ceiling for the same bytes: one bulk copy per cache and direction
+    kd_flat, vd_flat = kd[:nblk], vd[:nblk]
+
+    def bulk_step(i):
+        hk.copy_(kd_flat, non_blocking=True)
+        hv.copy_(vd_flat, non_blocking=True)
+        kd_flat.copy_(hk, non_blocking=True)
+        vd_flat.copy_(hv, non_blocking=True)
+
+    c_ms = time_graph_once(torch, stream, bulk_step, max(3, reps // 4))
+    ok = torch.equal(kd.view(torch.int16).cpu(), torch.from_numpy(batch.k_cache.view(np.int16)))
+    if world > 1:
+        k_ms, b_ms, c_ms = max_over_ranks([k_ms, b_ms, c_ms], "cuda")
+    line = {
+        "metric": "KV swap GB/s (GPU -> page-locked CPU pool -> GPU, Qwen3-8B layer)",
+        "value": whole_job_gbs(world, 2 * moved, k_ms), "unit": "GB/s", "n_gpus": world,
+        "steps": reps * GRAPH_STEPS, "warmup": 3, "ms_per_step": k_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": {"workload": "swap: 16 seqs x 4164 tokens, %d blocks of 16 (Hkv 8, D 128), out and back" % nblk,
+                   "bytes_each_way": moved, "l2": "inputs larger than L2 (%.0f MB each way)" % (moved / 1e6)},
+        "per_block_copies": {"ms_per_step": b_ms, "gbs": 2 * moved / (b_ms * 1e-3) / 1e9,
+                             "calls_per_step": 4 * nblk},
+        "bulk_copies": {"ms_per_step": c_ms, "gbs": 2 * moved / (c_ms * 1e-3) / 1e9, "calls_per_step": 4,
+                        "note": "contiguous blocks copied in bulk: the link's ceiling, not a block swap"},
+        "restored_bit_exact": bool(ok),
+        "clocks": clocks,
+        "gpu_launches": 2 * reps * GRAPH_STEPS,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def time_graph_once(torch, stream, fn, reps: int):
+    """Device time of one call of fn captured alone in a CUDA graph."""
+    with torch.cuda.stream(stream):
+        fn(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        fn(0)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def tables_bytes(lens, bs) -> int:
     return sum(workloads.cdiv(int(n), bs) for n in lens) * 4
 
@@ -843,7 +949,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["qwen3", "long", "gqa", "cow"], default="qwen3")
+    ap.add_argument("--config", choices=["qwen3", "long", "gqa", "cow", "swap"], default="qwen3")
     ap.add_argument("--copies", type=int, default=0,
                     help="cow: disjoint copies of the workload held on the device (default %d)" % COW_COPIES)
     ap.add_argument("--prefix-aware", action="store_true",
@@ -866,6 +972,8 @@ def main():
         return run_reference(args, rank, world)
     if args.config == "cow":
         return run_cow(args, rank, world, local_rank)
+    if args.config == "swap":
+        return run_swap(args, rank, world, local_rank)
     return run_ours(args, rank, world, local_rank)
 
 

@@ -108,6 +108,31 @@ PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *blo
                                 int head_dim, pa_dtype kv_dtype, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Block swap between two pools ("swap_blocks"), e.g. GPU cache <-> CPU pool.
+ * [P3] procedure steps 7-8 (a preempted request's blocks are copied to CPU
+ * memory and back) and the ablations (small blocks make swapping slow: many
+ * small transfers); [P4] section 12 (moving KV blocks of lower-priority
+ * requests to CPU memory, at block granularity).
+ *
+ *   src_k, src_v  [src_num_blocks, block_size, num_kv_heads, head_dim] pools
+ *   dst_k, dst_v  [dst_num_blocks, block_size, num_kv_heads, head_dim] pools
+ *                 Each may be device memory or page-locked host memory
+ *                 (cudaHostAlloc / cudaHostRegister, e.g. a pinned tensor);
+ *                 pageable host memory returns PA_ERR_INVALID_ARG.
+ *   block_mapping [num_pairs, 2] int64 (src id, dst id), device or
+ *                 page-locked host memory: block dst of dst_k / dst_v becomes
+ *                 a byte copy of block src of src_k / src_v. Pairs with an id
+ *                 outside its pool are skipped.
+ *   One kernel moves every pair (no per-block copy call). Destination
+ *   blocks must be distinct and must not overlap the sources.
+ *   num_pairs == 0 is a no-op. Asynchronous on `stream`.
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                                const int64_t *block_mapping, int num_pairs, int src_num_blocks,
+                                int dst_num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                pa_dtype kv_dtype, void *stream);
+
+/* ------------------------------------------------------------------------
  * Paged single-query (decode) attention.
  * [P4] section 8 (Attention(Q,K,V) = softmax(QK^T / sqrt(d)) V, unchanged by
  * paging) and section 14 (per step: read the block table, find each
@@ -386,6 +411,45 @@ PA_API pa_status pa_bm_refcount(const pa_bm *bm, int block, int *refcount);
 PA_API pa_status pa_bm_stats(const pa_bm *bm, pa_bm_stats_t *out);
 /* Free queue, front first (same cap / n convention as pa_bm_block_table). */
 PA_API pa_status pa_bm_free_list(const pa_bm *bm, int32_t *out, int cap, int *n);
+
+/* ------------------------------------------------------------------------
+ * Swapping to a CPU pool. [P3] procedure steps 7-8 (when no free block is
+ * left, a request's blocks are evicted all at once, sequences that share
+ * blocks -- the beams of one request -- together, and later copied back);
+ * [P4] section 12 (KV blocks of lower-priority requests moved to CPU memory).
+ *
+ * pa_bm_enable_swap gives the manager a CPU pool of num_host_blocks blocks
+ * (ids 0 .. num_host_blocks-1, an ascending free queue; once per handle).
+ *
+ * pa_bm_swap_out moves a group of resident sequences (each id once) to the
+ * CPU pool. The group must hold every reference to its blocks
+ * (PA_ERR_INVALID_ARG otherwise: a shared block cannot be half-evicted).
+ * Each distinct GPU block, in order of first appearance across the group's
+ * tables, gets the next CPU block; the pairs (GPU id, CPU id) are written to
+ * mapping[2*i], mapping[2*i+1] (cap pairs room; *num_pairs set). The GPU
+ * blocks return to the front of the free queue in that order, the tables
+ * hold the CPU ids, reference counts move with the blocks. The caller copies
+ * the data with pa_swap_blocks (GPU pool -> CPU pool) before the freed GPU
+ * blocks are written again.
+ *
+ * pa_bm_swap_in is the reverse: pairs (CPU id, GPU id), fresh GPU blocks
+ * from the free queue front, CPU blocks back to their queue front.
+ *
+ * Both are all-or-nothing: PA_ERR_OUT_OF_BLOCKS if the destination pool is
+ * short, PA_ERR_INVALID_ARG if cap is too small (nothing changes either way).
+ * While swapped out, pa_bm_append_slot and pa_bm_fork refuse the sequence
+ * (PA_ERR_INVALID_ARG); pa_bm_free releases its CPU blocks; pa_bm_stats
+ * still counts its tokens and logical blocks (used/shared/free count GPU
+ * blocks only).
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_bm_enable_swap(pa_bm *bm, int num_host_blocks);
+PA_API pa_status pa_bm_swap_out(pa_bm *bm, const int64_t *seqs, int num_seqs, int64_t *mapping, int cap,
+                                int *num_pairs);
+PA_API pa_status pa_bm_swap_in(pa_bm *bm, const int64_t *seqs, int num_seqs, int64_t *mapping, int cap,
+                               int *num_pairs);
+PA_API pa_status pa_bm_is_swapped(const pa_bm *bm, int64_t seq, int *swapped);
+PA_API pa_status pa_bm_swap_stats(const pa_bm *bm, int64_t *host_blocks, int64_t *free_host_blocks,
+                                  int64_t *swapped_seqs);
 
 #ifdef __cplusplus
 }

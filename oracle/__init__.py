@@ -20,7 +20,7 @@ import os
 import numpy as np
 
 from .build import build_oracle
-from .cache_ops import copy_blocks, reshape_and_cache, slot_mapping  # noqa: F401
+from .cache_ops import copy_blocks, reshape_and_cache, slot_mapping, swap_blocks  # noqa: F401
 from .block_manager_model import BlockManagerModel, OutOfBlocks  # noqa: F401
 
 _lib = None

@@ -15,10 +15,20 @@ What it follows:
     writer gets a clone, the original's count drops by one, only the
     writer's table changes.
 
+  * "PagedAttention, explained.", procedure steps 7-8 and "What Does
+    PagedAttention Actually Optimize?", section 12 (swapping): when blocks
+    run out, a request's blocks are evicted all at once -- sequences that
+    share blocks together -- copied to CPU memory, and copied back later.
+
 Readings where the pages are open: freed blocks go to the queue front in
 block-table order; a fork copies the parent's table and token count and adds
 one reference to each block; the free queue starts in ascending id order
-unless an explicit order is given.
+unless an explicit order is given. Swapping: the CPU pool is a second free
+queue (ascending ids, freed to the front); a swapped group must hold every
+reference to its blocks; each distinct block, in order of first appearance
+across the group's tables, takes the next block of the other pool, and the
+blocks it leaves go to the front of their queue in that order; a swapped-out
+sequence cannot grow or fork until it is swapped back in.
 """
 from __future__ import annotations
 
@@ -44,6 +54,9 @@ class BlockManagerModel:
         self.tables: Dict[int, List[int]] = {}
         self.tokens: Dict[int, int] = {}
         self.cow_copies = 0
+        self.host_free: Optional[List[int]] = None   # CPU pool, once swapping is enabled
+        self.host_ref: List[int] = []
+        self.swapped: set = set()
 
     # -- helpers ---------------------------------------------------------
     def _take(self) -> int:
@@ -68,6 +81,8 @@ class BlockManagerModel:
 
     def append_slot(self, seq: int) -> Tuple[int, int, int]:
         """Make room for one more token; returns (slot, cow_src, cow_dst)."""
+        if seq in self.swapped:
+            raise ValueError("sequence is swapped out")
         table = self.tables[seq]
         pos = self.tokens[seq]
         offset = pos % self.block_size
@@ -87,9 +102,9 @@ class BlockManagerModel:
         return slot, src, dst
 
     def fork(self, parent: int, child: int) -> None:
-        if child in self.tables:
-            raise KeyError("child exists")
         table = self.tables[parent]
+        if child in self.tables or parent in self.swapped:
+            raise ValueError("child exists or parent swapped out")
         for b in table:
             self.refcount[b] += 1
         self.tables[child] = list(table)
@@ -98,12 +113,67 @@ class BlockManagerModel:
     def free_seq(self, seq: int) -> None:
         table = self.tables.pop(seq)
         del self.tokens[seq]
+        ref, free = (self.host_ref, self.host_free) if seq in self.swapped else (self.refcount, self.free)
+        self.swapped.discard(seq)
         released = []
         for b in table:
-            self.refcount[b] -= 1
-            if self.refcount[b] == 0:
+            ref[b] -= 1
+            if ref[b] == 0:
                 released.append(b)
-        self.free[0:0] = released
+        free[0:0] = released
+
+    # -- swapping ----------------------------------------------------------
+    def enable_swap(self, num_host_blocks: int) -> None:
+        if self.host_free is not None or num_host_blocks <= 0:
+            raise ValueError("swap already enabled or empty pool")
+        self.host_free = list(range(num_host_blocks))
+        self.host_ref = [0] * num_host_blocks
+
+    def _swap(self, seqs, out: bool) -> List[Tuple[int, int]]:
+        if self.host_free is None:
+            raise ValueError("swap not enabled")
+        seqs = [int(x) for x in seqs]
+        for q in seqs:
+            if q not in self.tables:
+                raise KeyError("unknown sequence")
+        if len(set(seqs)) != len(seqs) or any((q in self.swapped) == out for q in seqs):
+            raise ValueError("duplicate sequence or wrong swap state")
+        order: List[int] = []
+        refs: Dict[int, int] = {}
+        for q in seqs:
+            for b in self.tables[q]:
+                if b not in refs:
+                    refs[b] = 0
+                    order.append(b)
+                refs[b] += 1
+        src_ref, dst_ref = (self.refcount, self.host_ref) if out else (self.host_ref, self.refcount)
+        src_free, dst_free = (self.free, self.host_free) if out else (self.host_free, self.free)
+        if any(src_ref[b] != refs[b] for b in order):
+            raise ValueError("a block is shared with a sequence outside the group")
+        if len(order) > len(dst_free):
+            raise OutOfBlocks("destination pool too small")
+        moved = {}
+        for b in order:
+            nb = dst_free.pop(0)
+            dst_ref[nb] = src_ref[b]
+            src_ref[b] = 0
+            moved[b] = nb
+        src_free[0:0] = order
+        for q in seqs:
+            self.tables[q] = [moved[b] for b in self.tables[q]]
+            if out:
+                self.swapped.add(q)
+            else:
+                self.swapped.discard(q)
+        return [(b, moved[b]) for b in order]
+
+    def swap_out(self, seqs) -> List[Tuple[int, int]]:
+        """Evict a group to the CPU pool; returns (GPU id, CPU id) pairs."""
+        return self._swap(seqs, True)
+
+    def swap_in(self, seqs) -> List[Tuple[int, int]]:
+        """Bring a group back; returns (CPU id, GPU id) pairs."""
+        return self._swap(seqs, False)
 
     # -- queries ---------------------------------------------------------
     def block_table(self, seq: int) -> List[int]:

@@ -16,6 +16,12 @@
   Eliminates KV-Cache Fragmentation", section "Advanced Memory Sharing and
   Copy-on-Write").
 
+* Swap (swap_blocks): a preempted request's blocks are copied whole to CPU
+  memory and back ("PagedAttention, explained.", procedure steps 7-8; "What
+  Does PagedAttention Actually Optimize?", section 12): block dst of the
+  destination pool becomes a copy of block src of the source pool. A pair
+  naming a block outside its pool is skipped (the library's convention).
+
 Arrays are numpy; the caches are [num_blocks, block_size, Hkv, D] and are
 modified in place.
 """
@@ -56,3 +62,14 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, block_mapping) -> None
     for src, dst in block_mapping:
         k_cache[int(dst)] = k_cache[int(src)]
         v_cache[int(dst)] = v_cache[int(src)]
+
+
+def swap_blocks(dst_k: np.ndarray, dst_v: np.ndarray, src_k: np.ndarray, src_v: np.ndarray,
+                block_mapping) -> None:
+    """For each (src, dst) pair, block dst of (dst_k, dst_v) becomes a copy of
+    block src of (src_k, src_v); pairs outside either pool are skipped."""
+    for src, dst in block_mapping:
+        src, dst = int(src), int(dst)
+        if 0 <= src < src_k.shape[0] and 0 <= dst < dst_k.shape[0]:
+            dst_k[dst] = src_k[src]
+            dst_v[dst] = src_v[src]

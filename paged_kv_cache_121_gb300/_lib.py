@@ -65,6 +65,13 @@ SIGNATURES = {
     "pa_bm_refcount": (c_int, [c_void_p, c_int, P_INT]),
     "pa_bm_stats": (c_int, [c_void_p, ctypes.POINTER(PaBmStats)]),
     "pa_bm_free_list": (c_int, [c_void_p, P_I32, c_int, P_INT]),
+    "pa_bm_enable_swap": (c_int, [c_void_p, c_int]),
+    "pa_bm_swap_out": (c_int, [c_void_p, P_I64, c_int, P_I64, c_int, P_INT]),
+    "pa_bm_swap_in": (c_int, [c_void_p, P_I64, c_int, P_I64, c_int, P_INT]),
+    "pa_bm_is_swapped": (c_int, [c_void_p, c_int64, P_INT]),
+    "pa_bm_swap_stats": (c_int, [c_void_p, P_I64, P_I64, P_I64]),
+    "pa_swap_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                               c_int, c_int, c_int, c_void_p]),
 }
 
 

@@ -126,6 +126,17 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, max_cont
                                 _stream(stream)), "pa_decode")
 
 
+def pa_swap_blocks(dst_k, dst_v, src_k, src_v, block_mapping, stream=None) -> None:
+    """Copy blocks block_mapping[i, 0] of (src_k, src_v) to blocks
+    block_mapping[i, 1] of (dst_k, dst_v); either pool may be a pinned host
+    tensor, the mapping a device or pinned host int64 tensor [n, 2]."""
+    snb, bs, hkv, d = _cache_dims(src_k)
+    dnb = int(dst_k.shape[0])
+    _check(_lib.load().pa_swap_blocks(_ptr(dst_k), _ptr(dst_v), _ptr(src_k), _ptr(src_v), _ptr(block_mapping),
+                                     int(block_mapping.shape[0]), snb, dnb, bs, hkv, d, _dtype(src_k),
+                                     _stream(stream)), "pa_swap_blocks")
+
+
 def pa_decode_shared_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                            max_context_len, shared_blocks) -> int:
     return int(_lib.load().pa_decode_shared_prefix_workspace_size(
@@ -286,3 +297,35 @@ class BlockManager:
         s = _lib.PaBmStats()
         _check(self._lib.pa_bm_stats(self._h, ctypes.byref(s)), "pa_bm_stats")
         return {name: int(getattr(s, name)) for name, _ in _lib.PaBmStats._fields_}
+
+    # -- swapping to a CPU pool -------------------------------------------
+    def enable_swap(self, num_host_blocks: int) -> None:
+        _check(self._lib.pa_bm_enable_swap(self._h, num_host_blocks), "pa_bm_enable_swap")
+
+    def _swap(self, fn, seqs) -> np.ndarray:
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        cap = int(sum(len(self.block_table(int(s))) for s in ids)) if ids.size else 0
+        out = np.zeros((max(cap, 1), 2), dtype=np.int64)
+        n = ctypes.c_int(0)
+        _check(fn(self._h, ids.ctypes.data_as(_lib.P_I64), ids.size, out.ctypes.data_as(_lib.P_I64), cap,
+                  ctypes.byref(n)), fn.__name__)
+        return out[: n.value].copy()
+
+    def swap_out(self, seqs) -> np.ndarray:
+        """Move a group of sequences to the CPU pool; returns [n, 2] (GPU id, CPU id) pairs."""
+        return self._swap(self._lib.pa_bm_swap_out, seqs)
+
+    def swap_in(self, seqs) -> np.ndarray:
+        """Bring a swapped-out group back; returns [n, 2] (CPU id, GPU id) pairs."""
+        return self._swap(self._lib.pa_bm_swap_in, seqs)
+
+    def is_swapped(self, seq: int) -> bool:
+        v = ctypes.c_int(0)
+        _check(self._lib.pa_bm_is_swapped(self._h, seq, ctypes.byref(v)), "pa_bm_is_swapped")
+        return bool(v.value)
+
+    def swap_stats(self) -> dict:
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(self._lib.pa_bm_swap_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+               "pa_bm_swap_stats")
+        return {"host_blocks": a.value, "free_host_blocks": b.value, "swapped_seqs": c.value}

@@ -529,6 +529,41 @@ PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *blo
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// The address a kernel uses for p: device memory as is; page-locked host
+// memory through its device mapping. Pageable host memory gives nullptr.
+static const void *device_view(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    return nullptr;
+}
+
+PA_API pa_status pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                                const int64_t *block_mapping, int num_pairs, int src_num_blocks,
+                                int dst_num_blocks, int block_size, int num_kv_heads, int head_dim,
+                                pa_dtype kv_dtype, void *stream) {
+    if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || !valid_dtype(kv_dtype))
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!dst_k || !dst_v || !src_k || !src_v || !block_mapping) return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes =
+        static_cast<int64_t>(block_size) * num_kv_heads * head_dim * element_bytes(kv_dtype);
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    void *dk = const_cast<void *>(device_view(dst_k)), *dv = const_cast<void *>(device_view(dst_v));
+    const void *sk = device_view(src_k), *sv = device_view(src_v), *bm = device_view(block_mapping);
+    if (!dk || !dv || !sk || !sv || !bm) return PA_ERR_INVALID_ARG;
+    if (!aligned16(dk) || !aligned16(dv) || !aligned16(sk) || !aligned16(sv)) return PA_ERR_INVALID_ARG;
+    cudaError_t e = launch_transfer_blocks(dk, dv, sk, sv, static_cast<const int64_t *>(bm), num_pairs,
+                                           src_num_blocks, dst_num_blocks, block_bytes, as_stream(stream));
+    if (e == cudaErrorInvalidValue) return PA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                        int block_size, int max_context_len) {
     const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,

@@ -13,6 +13,14 @@
 // "Copy-on-write"; "How PagedAttention Eliminates KV-Cache Fragmentation",
 // section "Advanced Memory Sharing and Copy-on-Write". Each CTA copies one
 // 8 KiB chunk of one block of one cache with 16-byte vectors.
+//
+// swap_blocks: the same whole-block copy between two pools, either of which
+// may be page-locked host memory -- preempted sequences' blocks are moved to
+// CPU memory and back ("PagedAttention, explained.", procedure steps 7 and 8;
+// "What Does PagedAttention Actually Optimize?", section 12). The pages note
+// that swapping small blocks is slow because it means many small transfers;
+// here one kernel moves every block of the request, each CTA streaming an
+// 8 KiB chunk over the CPU-GPU link with 16-byte accesses.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -54,34 +62,53 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
 constexpr int kCopyChunkVecs = 512;  // 8 KiB per CTA
 
 __global__ void __launch_bounds__(256)
-copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
-                   const int64_t *__restrict__ block_mapping, int64_t num_blocks,
-                   int64_t block_vecs) {
+transfer_blocks_kernel(uint4 *__restrict__ dst_k, uint4 *__restrict__ dst_v, const uint4 *__restrict__ src_k,
+                       const uint4 *__restrict__ src_v, const int64_t *__restrict__ block_mapping,
+                       int64_t src_blocks, int64_t dst_blocks, int64_t block_vecs) {
     const int pair = blockIdx.x;
     const int which = blockIdx.y & 1;
     const int64_t chunk = blockIdx.y >> 1;
     const int64_t src = block_mapping[2 * static_cast<int64_t>(pair)];
     const int64_t dst = block_mapping[2 * static_cast<int64_t>(pair) + 1];
-    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return;
-    uint4 *base = which ? v_cache : k_cache;
-    const uint4 *s = base + src * block_vecs;
-    uint4 *d = base + dst * block_vecs;
+    if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) return;
+    const uint4 *s = (which ? src_v : src_k) + src * block_vecs;
+    uint4 *d = (which ? dst_v : dst_k) + dst * block_vecs;
     const int64_t c0 = chunk * kCopyChunkVecs;
     const int64_t c1 = c0 + kCopyChunkVecs < block_vecs ? c0 + kCopyChunkVecs : block_vecs;
-    for (int64_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) d[c] = s[c];
+    // all loads of the chunk in flight before the stores (the source may be
+    // host memory across the CPU-GPU link)
+    constexpr int kPer = kCopyChunkVecs / 256;
+    uint4 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int64_t c = c0 + threadIdx.x + j * 256;
+        if (c < c1) v[j] = s[c];
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int64_t c = c0 + threadIdx.x + j * 256;
+        if (c < c1) d[c] = v[j];
+    }
+}
+
+cudaError_t launch_transfer_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                                   const int64_t *block_mapping, int num_pairs, int64_t src_blocks,
+                                   int64_t dst_blocks, int64_t block_bytes, cudaStream_t stream) {
+    const int64_t block_vecs = block_bytes / 16;
+    const int64_t chunks = (block_vecs + kCopyChunkVecs - 1) / kCopyChunkVecs;
+    if (chunks * 2 > 65535) return cudaErrorInvalidValue;
+    dim3 grid(num_pairs, static_cast<unsigned>(chunks * 2));
+    transfer_blocks_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<uint4 *>(dst_k), static_cast<uint4 *>(dst_v), static_cast<const uint4 *>(src_k),
+        static_cast<const uint4 *>(src_v), block_mapping, src_blocks, dst_blocks, block_vecs);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
                                int num_pairs, int64_t num_blocks, int64_t block_bytes,
                                cudaStream_t stream) {
-    const int64_t block_vecs = block_bytes / 16;
-    const int64_t chunks = (block_vecs + kCopyChunkVecs - 1) / kCopyChunkVecs;
-    if (chunks * 2 > 65535) return cudaErrorInvalidValue;
-    dim3 grid(num_pairs, static_cast<unsigned>(chunks * 2));
-    copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(k_cache),
-                                                 static_cast<uint4 *>(v_cache), block_mapping,
-                                                 num_blocks, block_vecs);
-    return cudaGetLastError();
+    return launch_transfer_blocks(k_cache, v_cache, k_cache, v_cache, block_mapping, num_pairs, num_blocks,
+                                  num_blocks, block_bytes, stream);
 }
 
 }  // namespace pa

@@ -56,6 +56,10 @@ struct DecodeCall {
 // than scratch_bytes.
 int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes, void *stream);
 
+cudaError_t launch_transfer_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
+                                   const int64_t *block_mapping, int num_pairs, int64_t src_blocks,
+                                   int64_t dst_blocks, int64_t block_bytes, cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
                                int num_pairs, int64_t num_blocks, int64_t block_bytes,
                                cudaStream_t stream);

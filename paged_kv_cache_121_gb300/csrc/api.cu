@@ -81,6 +81,7 @@ int env_int(const char *name, int lo, int hi) {
 //   PA_DECODE_CTAS_PER_SM  CTAs per SM the split plan aims at
 //   PA_DECODE_HEADS        KV heads per tensor-core CTA (1..8)
 //   PA_DECODE_RING_KB      shared-memory ring per tensor-core CTA (KiB)
+//   PA_PREFIX_KERNEL       "mma": shared-prefix pass on mma.sync (default: tcgen05)
 int ctas_per_sm_override() {
     static const int v = env_int("PA_DECODE_CTAS_PER_SM", 1, 64);
     return v;
@@ -88,6 +89,14 @@ int ctas_per_sm_override() {
 int heads_cap() {
     static const int v = env_int("PA_DECODE_HEADS", 1, 8);
     return v ? v : kMmaHeadsPerCta;
+}
+// PA_PREFIX_KERNEL=mma runs the shared-prefix pass on mma.sync instead of tcgen05.
+bool prefix_tc_enabled() {
+    static const bool v = [] {
+        const char *e = std::getenv("PA_PREFIX_KERNEL");
+        return !(e && std::strcmp(e, "mma") == 0);
+    }();
+    return v;
 }
 int ring_kb() {
     static const int v = env_int("PA_DECODE_RING_KB", 16, 200);
@@ -111,10 +120,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // first as (dim within a 64-dim half, token, half, head, block): the strides
 // of the middle three are permuted so that a box of 64 dims x box_tokens
 // tokens x every half x box_heads heads lands in shared memory as
-// [head][half][token][128 bytes]. 128-byte swizzle; out-of-range
-// coordinates read as zeros.
+// [head][half][token][128 bytes] (box_halves 0: every half). 128-byte
+// swizzle; out-of-range coordinates read as zeros.
 pa_status make_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int64_t block_size,
-                         int num_kv_heads, int head_dim, int box_tokens, int box_heads) {
+                         int num_kv_heads, int head_dim, int box_tokens, int box_heads, int box_halves = 0) {
     auto enc = tensor_map_encoder();
     if (!enc) return PA_ERR_CUDA;
     const cuuint64_t halves = static_cast<cuuint64_t>(head_dim / 64);
@@ -122,7 +131,8 @@ pa_status make_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks
                                 static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
     const cuuint64_t strides[4] = {row * num_kv_heads, 128, row, row * num_kv_heads * block_size};
-    const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(box_tokens), static_cast<cuuint32_t>(halves),
+    const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(box_tokens),
+                               static_cast<cuuint32_t>(box_halves > 0 ? box_halves : static_cast<int>(halves)),
                                static_cast<cuuint32_t>(box_heads), 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims, strides,
@@ -375,7 +385,8 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
 // form, both merged by the log-sum-exp merge.
 // ---------------------------------------------------------------------------
 struct PrefixPlan {
-    int prefix_tokens;   // shared tokens attended by the prefix pass (a multiple of 16)
+    bool tc;             // prefix pass on tcgen05 (else mma.sync)
+    int prefix_tokens;   // shared tokens attended by the prefix pass (whole tiles)
     int chunk_tokens;
     int chunks;          // prefix partitions (grid.x of the prefix pass)
     int row_groups;      // grid.z of the prefix pass
@@ -383,22 +394,28 @@ struct PrefixPlan {
     int part_stride;     // partitions per (sequence, head): chunks + suffix splits
 };
 
-PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms) {
+PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms, bool tc) {
     PrefixPlan pp{};
+    pp.tc = tc;
+    // the prefix pass takes whole tiles; shared tokens past the last one go with the rest
+    const int tile = tc ? prefix_tc_tile_tokens() : 16;
     int64_t P = std::min<int64_t>(static_cast<int64_t>(shared_blocks) * s.block_size, s.max_ctx);
-    P = P / 16 * 16;   // whole 16-token tiles (blocks of 8: an odd last block goes to the rest)
+    P = P / tile * tile;
     pp.prefix_tokens = static_cast<int>(P);
     const int group = s.num_heads / s.num_kv_heads;
-    pp.row_groups = static_cast<int>(cdiv64(static_cast<int64_t>(s.num_seqs) * group, prefix_rows_per_cta()));
+    const int rows = tc ? prefix_tc_rows_per_cta() : prefix_rows_per_cta();
+    pp.row_groups = static_cast<int>(cdiv64(static_cast<int64_t>(s.num_seqs) * group, rows));
     if (P > 0) {
         const int64_t per_chunk = static_cast<int64_t>(s.num_kv_heads) * pp.row_groups;
-        const int64_t cap = static_cast<int64_t>(sms) * kCtasPerSmMma;
+        const int64_t cap = static_cast<int64_t>(sms) * (tc ? 1 : kCtasPerSmMma);
         int64_t chunks = std::max<int64_t>(1, cap / per_chunk);
-        chunks = std::min<int64_t>(chunks, std::max<int64_t>(1, P / kMinPrefixChunk));
+        chunks = std::min<int64_t>(chunks, std::max<int64_t>(1, P / std::max(kMinPrefixChunk, tile)));
         chunks = std::min<int64_t>(chunks, kMaxSplits);
-        const int64_t tiles = P / 16;
-        const int64_t ct = cdiv64(tiles, chunks);
-        pp.chunk_tokens = static_cast<int>(ct * 16);
+        const int64_t tiles = P / tile;
+        int64_t ct = cdiv64(tiles, chunks);
+        if (tc)   // a chunk's block ids must fit the kernel's staging array
+            ct = std::min<int64_t>(ct, std::max<int64_t>(1, (static_cast<int64_t>(kTcChunkBlocks - 1) * s.block_size) / tile));
+        pp.chunk_tokens = static_cast<int>(ct * tile);
         pp.chunks = static_cast<int>(cdiv64(tiles, ct));
     }
     DecodeShape rest = s;
@@ -632,7 +649,7 @@ PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads
     if (current_device(&dev) != PA_OK) return 0;
     const int sms = sm_count(dev);
     if (sms <= 0) return 0;
-    const PrefixPlan pp = plan_prefix(s, shared_blocks, sms);
+    const PrefixPlan pp = plan_prefix(s, shared_blocks, sms, prefix_tc_enabled());
     const size_t plain = workspace_layout(s, plan_split(s, sms, true)).total;
     return std::max(prefix_workspace(s, pp).total, plain);
 }
@@ -657,7 +674,7 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     if ((st = current_device(&dev)) != PA_OK) return st;
     const int sms = sm_count(dev);
     if (sms <= 0) return PA_ERR_CUDA;
-    const PrefixPlan pp = plan_prefix(s, shared_blocks, sms);
+    const PrefixPlan pp = plan_prefix(s, shared_blocks, sms, prefix_tc_enabled());
     if (pp.chunks == 0)   // nothing shared in whole tiles: the plain decode
         return decode_planned(s, out, out_dtype, query, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
                               context_lens, 0, scale, workspace, workspace_bytes, stream);
@@ -690,19 +707,31 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     pq.prefix_tokens = pp.prefix_tokens;
     pq.chunk_tokens = pp.chunk_tokens;
     pq.part_stride = pp.part_stride;
-    const int stage = prefix_stage_bytes(head_dim);
-    pq.ring_bytes = std::max(stage, std::min(kPrefixMaxRingBytes, ring_kb() * 1024) / stage * stage);
     pq.scale_log2 = scale * kLog2e;
     {
-        const int box = decode_mma_box_tokens(block_size);
-        CUtensorMap tk, tv;
-        if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK)
-            return st;
-        if ((st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK)
-            return st;
         const dim3 grid(static_cast<unsigned>(pp.chunks), static_cast<unsigned>(num_kv_heads),
                         static_cast<unsigned>(pp.row_groups));
-        if (launch_prefix_mma(pq, tk, tv, grid, strm) != cudaSuccess) return PA_ERR_CUDA;
+        CUtensorMap tk, tv;
+        if (pp.tc) {
+            // boxes of one block (up to a 64-token tile), one 64-dim half, one head
+            const int box = std::min(block_size, prefix_tc_tile_tokens());
+            const int stage = prefix_tc_stage_bytes(head_dim);
+            pq.ring_bytes = std::max(stage, std::min(kTcMaxRingBytes, ring_kb() * 1024) / stage * stage);
+            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1)) != PA_OK)
+                return st;
+            if ((st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1)) != PA_OK)
+                return st;
+            if (launch_prefix_tc(pq, tk, tv, grid, strm) != cudaSuccess) return PA_ERR_CUDA;
+        } else {
+            const int box = decode_mma_box_tokens(block_size);
+            const int stage = prefix_stage_bytes(head_dim);
+            pq.ring_bytes = std::max(stage, std::min(kPrefixMaxRingBytes, ring_kb() * 1024) / stage * stage);
+            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK)
+                return st;
+            if ((st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK)
+                return st;
+            if (launch_prefix_mma(pq, tk, tv, grid, strm) != cudaSuccess) return PA_ERR_CUDA;
+        }
     }
     // 2. the rest of every context (the tokens past the shared ones)
     DecodeParams p;

@@ -25,6 +25,14 @@ int prefix_rows_per_cta();
 int prefix_stage_bytes(int head_dim);
 cudaError_t launch_prefix_mma(const PrefixParams &p, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                               dim3 grid, cudaStream_t stream);
+// Shared-prefix pass on tcgen05 (prefix_tc.cu): grid (chunks, Hkv, row groups of 128).
+constexpr int kTcMaxRingBytes = 128 * 1024;
+constexpr int kTcChunkBlocks = 256;   // most block ids one chunk of the tcgen05 pass may span
+int prefix_tc_rows_per_cta();
+int prefix_tc_tile_tokens();
+int prefix_tc_stage_bytes(int head_dim);
+cudaError_t launch_prefix_tc(const PrefixParams &p, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                             dim3 grid, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
                              const float *exp_sums, const int32_t *context_lens, int num_seqs,

@@ -31,6 +31,7 @@ constexpr int kContiguousTile = 16;   // tokens per tile of a contiguous cache
 constexpr int kMmaRingKiB = 96;       // shared-memory ring per tensor-core CTA
 constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
 constexpr int kMinPrefixChunk = 64;   // tokens per chunk of the shared-prefix pass, at least
+constexpr int kMinRestSplitTokens = 64;   // partitions of the rest of a shared-prefix context, at least
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int *> g_status_addr[kMaxDevices];
@@ -82,6 +83,7 @@ int env_int(const char *name, int lo, int hi) {
 //   PA_DECODE_HEADS        KV heads per tensor-core CTA (1..8)
 //   PA_DECODE_RING_KB      shared-memory ring per tensor-core CTA (KiB)
 //   PA_PREFIX_KERNEL       "mma": shared-prefix pass on mma.sync (default: tcgen05)
+//   PA_PREFIX_OVERLAP      "0": shared-prefix pass not overlapped with the rest
 int ctas_per_sm_override() {
     static const int v = env_int("PA_DECODE_CTAS_PER_SM", 1, 64);
     return v;
@@ -90,6 +92,29 @@ int heads_cap() {
     static const int v = env_int("PA_DECODE_HEADS", 1, 8);
     return v ? v : kMmaHeadsPerCta;
 }
+// PA_PREFIX_OVERLAP=0 runs the shared-prefix pass and the rest-of-context
+// decode one after the other on the caller's stream instead of side by side.
+bool prefix_overlap_enabled() {
+    static const bool v = [] {
+        const char *e = std::getenv("PA_PREFIX_OVERLAP");
+        return !(e && std::strcmp(e, "0") == 0);
+    }();
+    return v;
+}
+
+// A second stream per (device, host thread), created on first use: the
+// shared-prefix pass runs there alongside the rest-of-context decode,
+// ordered against the caller's stream by events (capturable into a graph).
+cudaStream_t side_stream(int dev) {
+    thread_local cudaStream_t streams[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        streams[dev] = nullptr;
+    }
+    return streams[dev];
+}
+
 // PA_PREFIX_KERNEL=mma runs the shared-prefix pass on mma.sync instead of tcgen05.
 bool prefix_tc_enabled() {
     static const bool v = [] {
@@ -178,7 +203,7 @@ int split_granule(const DecodeShape &s, bool mma) { return mma ? decode_mma_tile
 // Split each (sequence, KV-head group, head tile) context so that about
 // sm_count * ctas_per_sm CTAs exist, with at least kMinSplitTokens per piece.
 // Partitions are whole granules, sized evenly over max_context_len.
-Plan plan_split(const DecodeShape &s, int sms, bool mma) {
+Plan plan_split(const DecodeShape &s, int sms, bool mma, int min_split_tokens = kMinSplitTokens) {
     Plan pl;
     pl.mma = mma;
     pl.heads_per_cta = mma ? decode_mma_heads_per_cta(s.num_kv_heads, heads_cap()) : 1;
@@ -193,7 +218,7 @@ Plan plan_split(const DecodeShape &s, int sms, bool mma) {
     int64_t nsplit = 1;
     if (units > 0 && units < cap) {
         nsplit = cap / units;
-        const int64_t min_pg = std::max<int64_t>(1, cdiv64(kMinSplitTokens, gran));
+        const int64_t min_pg = std::max<int64_t>(1, cdiv64(min_split_tokens, gran));
         nsplit = std::min(nsplit, std::max<int64_t>(1, ngran / min_pg));
         nsplit = std::min<int64_t>(nsplit, kMaxSplits);
     }
@@ -420,8 +445,13 @@ PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms, bool tc
     }
     DecodeShape rest = s;
     rest.max_ctx = static_cast<int>(std::max<int64_t>(0, s.max_ctx - P));
-    pp.suffix = plan_split(rest, sms, true);
+    // the merge kernel runs anyway: the rest may be cut finer than a plain decode's
+    pp.suffix = plan_split(rest, sms, true, kMinRestSplitTokens);
     pp.suffix.cluster = false;
+    if (pp.suffix.nsplit > 1) {   // partitions of the rest, in whole tiles, without the cluster's rounding
+        const int64_t ngran = std::max<int64_t>(1, cdiv64(rest.max_ctx, 16));
+        pp.suffix.nsplit = static_cast<int>(cdiv64(ngran, cdiv64(pp.suffix.part_tokens, 16)));
+    }
     pp.part_stride = pp.chunks + pp.suffix.nsplit;   // the rest's partitions follow the prefix chunks
     return pp;
 }
@@ -687,6 +717,33 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     float *max_logits = reinterpret_cast<float *>(ws + wl.ml_off);
     float *exp_sums = reinterpret_cast<float *>(ws + wl.count_off);
     cudaStream_t strm = as_stream(stream);
+    // The prefix pass and the rest-of-context decode write disjoint partitions:
+    // the prefix pass runs on a side stream forked from (and joined back into)
+    // the caller's stream, the rest on the caller's stream, then the merge.
+    cudaStream_t pstrm = strm;
+    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+    if (prefix_overlap_enabled()) {
+        cudaStream_t side = side_stream(dev);
+        if (side && cudaEventCreateWithFlags(&fork_ev, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&join_ev, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventRecord(fork_ev, strm) == cudaSuccess && cudaStreamWaitEvent(side, fork_ev, 0) == cudaSuccess) {
+            pstrm = side;
+        } else {
+            cudaGetLastError();
+            if (fork_ev) cudaEventDestroy(fork_ev);
+            if (join_ev) cudaEventDestroy(join_ev);
+            fork_ev = join_ev = nullptr;
+        }
+    }
+    auto join = [&]() -> bool {   // the caller's stream waits for the side stream's work
+        if (pstrm == strm) return true;
+        const bool ok = cudaEventRecord(join_ev, pstrm) == cudaSuccess &&
+                        cudaStreamWaitEvent(strm, join_ev, 0) == cudaSuccess;
+        cudaEventDestroy(fork_ev);
+        cudaEventDestroy(join_ev);
+        pstrm = strm;
+        return ok;
+    };
 
     // 1. the shared prefix, once for every row
     PrefixParams pq;
@@ -717,20 +774,28 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
             const int box = std::min(block_size, prefix_tc_tile_tokens());
             const int stage = prefix_tc_stage_bytes(head_dim);
             pq.ring_bytes = std::max(stage, std::min(kTcMaxRingBytes, ring_kb() * 1024) / stage * stage);
-            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1)) != PA_OK)
+            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1)) != PA_OK ||
+                (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1)) != PA_OK) {
+                join();
                 return st;
-            if ((st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1)) != PA_OK)
-                return st;
-            if (launch_prefix_tc(pq, tk, tv, grid, strm) != cudaSuccess) return PA_ERR_CUDA;
+            }
+            if (launch_prefix_tc(pq, tk, tv, grid, pstrm) != cudaSuccess) {
+                join();
+                return PA_ERR_CUDA;
+            }
         } else {
             const int box = decode_mma_box_tokens(block_size);
             const int stage = prefix_stage_bytes(head_dim);
             pq.ring_bytes = std::max(stage, std::min(kPrefixMaxRingBytes, ring_kb() * 1024) / stage * stage);
-            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK)
+            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK ||
+                (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK) {
+                join();
                 return st;
-            if ((st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK)
-                return st;
-            if (launch_prefix_mma(pq, tk, tv, grid, strm) != cudaSuccess) return PA_ERR_CUDA;
+            }
+            if (launch_prefix_mma(pq, tk, tv, grid, pstrm) != cudaSuccess) {
+                join();
+                return PA_ERR_CUDA;
+            }
         }
     }
     // 2. the rest of every context (the tokens past the shared ones)
@@ -748,7 +813,9 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     // split-K partitions after the prefix chunks, then the merge
     p.part_offset = pp.chunks;
     p.mode = kModeSplitK;
-    if ((st = launch_decode(s, p, kv_dtype, true, dev, strm)) != PA_OK) return st;
+    st = launch_decode(s, p, kv_dtype, true, dev, strm);
+    if (!join() && st == PA_OK) st = PA_ERR_CUDA;
+    if (st != PA_OK) return st;
     // 3. merge all partitions of every row
     const cudaError_t e = launch_lse_merge(out, out_dtype == PA_BF16 ? 1 : 0, tmp_out, max_logits, exp_sums,
                                            context_lens, num_seqs, num_heads, head_dim, pp.part_stride, 0, strm);

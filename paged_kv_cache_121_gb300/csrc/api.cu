@@ -32,6 +32,7 @@ constexpr int kMmaRingKiB = 96;       // shared-memory ring per tensor-core CTA
 constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
 constexpr int kMinPrefixChunk = 64;   // tokens per chunk of the shared-prefix pass, at least
 constexpr int kMinRestSplitTokens = 64;   // partitions of the rest of a shared-prefix context, at least
+constexpr int kRestCtasPerSm = 3;         // the rest's split aims past one wave: CTAs of short rests end early
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int *> g_status_addr[kMaxDevices];
@@ -203,7 +204,8 @@ int split_granule(const DecodeShape &s, bool mma) { return mma ? decode_mma_tile
 // Split each (sequence, KV-head group, head tile) context so that about
 // sm_count * ctas_per_sm CTAs exist, with at least kMinSplitTokens per piece.
 // Partitions are whole granules, sized evenly over max_context_len.
-Plan plan_split(const DecodeShape &s, int sms, bool mma, int min_split_tokens = kMinSplitTokens) {
+Plan plan_split(const DecodeShape &s, int sms, bool mma, int min_split_tokens = kMinSplitTokens,
+                int ctas_per_sm = 0) {
     Plan pl;
     pl.mma = mma;
     pl.heads_per_cta = mma ? decode_mma_heads_per_cta(s.num_kv_heads, heads_cap()) : 1;
@@ -213,7 +215,9 @@ Plan plan_split(const DecodeShape &s, int sms, bool mma, int min_split_tokens = 
         static_cast<int64_t>(s.num_seqs) * (s.num_kv_heads / pl.heads_per_cta) * pl.ntile;
     const int gran = split_granule(s, mma);
     const int64_t ngran = std::max<int64_t>(1, cdiv64(s.max_ctx, gran));
-    const int per_sm = ctas_per_sm_override() ? ctas_per_sm_override() : (mma ? kCtasPerSmMma : kCtasPerSmSimt);
+    const int per_sm = ctas_per_sm_override() ? ctas_per_sm_override()
+                       : ctas_per_sm > 0      ? ctas_per_sm
+                                              : (mma ? kCtasPerSmMma : kCtasPerSmSimt);
     const int64_t cap = static_cast<int64_t>(sms) * per_sm;
     int64_t nsplit = 1;
     if (units > 0 && units < cap) {
@@ -446,7 +450,7 @@ PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms, bool tc
     DecodeShape rest = s;
     rest.max_ctx = static_cast<int>(std::max<int64_t>(0, s.max_ctx - P));
     // the merge kernel runs anyway: the rest may be cut finer than a plain decode's
-    pp.suffix = plan_split(rest, sms, true, kMinRestSplitTokens);
+    pp.suffix = plan_split(rest, sms, true, kMinRestSplitTokens, kRestCtasPerSm);
     pp.suffix.cluster = false;
     if (pp.suffix.nsplit > 1) {   // partitions of the rest, in whole tiles, without the cluster's rounding
         const int64_t ngran = std::max<int64_t>(1, cdiv64(rest.max_ctx, 16));

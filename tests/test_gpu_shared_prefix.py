@@ -137,3 +137,30 @@ def test_shared_prefix_cow_workload(prefix_len):
     db = DeviceBatch(batch)
     out = run_shared(db, shared)
     assert max_err(out, oracle_out(batch)) <= ATOL
+
+
+def test_shared_prefix_in_a_cuda_graph_matches_eager():
+    """The prefix pass runs on a side stream forked from the caller's stream;
+    captured into a CUDA graph (as a serving loop would) and replayed, the
+    call gives the eager result."""
+    batch = workloads.shared_prefix_batch("sp", 32, tuple(range(5, 400, 25)), 32, 8, 128, 32, seed_values=830)
+    db = DeviceBatch(batch)
+    n = pa.pa_decode_shared_prefix_workspace_size(batch.num_seqs, 32, 8, 128, 32, batch.max_context_len, 32)
+    ws = torch.zeros(max(n, 1), dtype=torch.uint8, device="cuda")
+    eager = run_shared(db, 32, workspace=ws)
+    out = torch.zeros_like(eager)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        pa.pa_decode_shared_prefix(out, db.query, db.k_cache, db.v_cache, db.block_tables, db.context_lens,
+                                   batch.max_context_len, 32, batch.scale, ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        pa.pa_decode_shared_prefix(out, db.query, db.k_cache, db.v_cache, db.block_tables, db.context_lens,
+                                   batch.max_context_len, 32, batch.scale, ws)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    assert max_err(out, oracle_out(batch)) <= ATOL
+    assert pa.pa_device_status(clear=True) == 0

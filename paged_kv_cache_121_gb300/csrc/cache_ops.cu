@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "device_common.cuh"
 #include "internal.h"
 
 namespace pa {
@@ -32,6 +33,8 @@ __global__ void __launch_bounds__(128)
 reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
                          uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                          const int64_t *__restrict__ slot_mapping, int64_t num_slots, int row_vecs) {
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int i = blockIdx.x;
     const int64_t slot = slot_mapping[i];
     if (slot < 0 || slot >= num_slots) return;
@@ -52,11 +55,10 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
                                      int64_t num_slots, int row_bytes, cudaStream_t stream) {
     const int row_vecs = row_bytes / 16;
     const int threads = row_vecs >= 128 ? 128 : ((row_vecs + 31) / 32) * 32;
-    reshape_and_cache_kernel<<<num_tokens, threads, 0, stream>>>(
-        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_slots,
-        row_vecs);
-    return cudaGetLastError();
+    return launch_kernel(reshape_and_cache_kernel, dim3(num_tokens), dim3(threads), 0, stream, 1u,
+                         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+                         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping,
+                         num_slots, row_vecs);
 }
 
 constexpr int kCopyChunkVecs = 512;  // 8 KiB per CTA
@@ -65,6 +67,8 @@ __global__ void __launch_bounds__(256)
 transfer_blocks_kernel(uint4 *__restrict__ dst_k, uint4 *__restrict__ dst_v, const uint4 *__restrict__ src_k,
                        const uint4 *__restrict__ src_v, const int64_t *__restrict__ block_mapping,
                        int64_t src_blocks, int64_t dst_blocks, int64_t block_vecs) {
+    grid_dependency_wait();
+    grid_dependents_launch();
     const int pair = blockIdx.x;
     const int which = blockIdx.y & 1;
     const int64_t chunk = blockIdx.y >> 1;
@@ -98,10 +102,9 @@ cudaError_t launch_transfer_blocks(void *dst_k, void *dst_v, const void *src_k, 
     const int64_t chunks = (block_vecs + kCopyChunkVecs - 1) / kCopyChunkVecs;
     if (chunks * 2 > 65535) return cudaErrorInvalidValue;
     dim3 grid(num_pairs, static_cast<unsigned>(chunks * 2));
-    transfer_blocks_kernel<<<grid, 256, 0, stream>>>(
-        static_cast<uint4 *>(dst_k), static_cast<uint4 *>(dst_v), static_cast<const uint4 *>(src_k),
-        static_cast<const uint4 *>(src_v), block_mapping, src_blocks, dst_blocks, block_vecs);
-    return cudaGetLastError();
+    return launch_kernel(transfer_blocks_kernel, grid, dim3(256), 0, stream, 1u, static_cast<uint4 *>(dst_k),
+                         static_cast<uint4 *>(dst_v), static_cast<const uint4 *>(src_k),
+                         static_cast<const uint4 *>(src_v), block_mapping, src_blocks, dst_blocks, block_vecs);
 }
 
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,

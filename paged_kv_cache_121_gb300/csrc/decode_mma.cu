@@ -210,6 +210,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tile = blockIdx.y % p.ntile;
     const int b = blockIdx.z;
     const int rows = min(kRowsPerTile, p.group - tile * kRowsPerTile);
+    grid_dependency_wait();   // the previous kernel on the stream (e.g. the scatter) is complete
     const SeqWork w = seq_work(p, b, part);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // (one instantiation per epilogue keeps the other's registers out of the loop)
@@ -392,31 +393,19 @@ static cudaError_t launch_impl(const DecodeParams &p, const CUtensorMap &tk, con
                                dim3 grid, cudaStream_t stream) {
     using C = MmaCfg<D, TT>;
     const size_t smem = C::smem_bytes(p.ring_bytes);
+    const dim3 block(32 * (p.heads_per_cta + 1));
     if (!p.cluster_merge) {
         auto kern = decode_mma_kernel<D, TT, false, kPairs>;
         static unsigned long long done = 0;
         cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
         if (e != cudaSuccess) return e;
-        kern<<<grid, 32 * (p.heads_per_cta + 1), smem, stream>>>(tk, tv, p);
-        return cudaGetLastError();
+        return launch_kernel(kern, grid, block, smem, stream, 1u, tk, tv, p);
     }
     auto kern = decode_mma_kernel<D, TT, true, kPairs>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(32 * (p.heads_per_cta + 1));
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = grid.x;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+    return launch_kernel(kern, grid, block, smem, stream, grid.x, tk, tv, p);
 }
 
 bool decode_mma_supported(int head_dim, int block_size) {

@@ -64,6 +64,7 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     const int tile = blockIdx.y % p.ntile;
     const int b = blockIdx.z;
     const int rows = min(kRowsPerTile, p.group - tile * kRowsPerTile);
+    grid_dependency_wait();
     const SeqWork w = seq_work(p, b, part);
     if (w.tok_begin >= w.tok_end) {
         write_empty<D>(p, b, g, tile, part, rows, w.nparts);
@@ -140,6 +141,7 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     }
     __syncthreads();
     combine_warps<D>(smem_f, kWarps, rows);
+    grid_dependents_launch();
     write_result<D>(p, smem_f, kWarps, b, g, tile, part, rows);
 }
 
@@ -150,8 +152,7 @@ static cudaError_t launch_simt_impl(const DecodeParams &p, dim3 grid, cudaStream
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, smem, done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, 128, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, dim3(128), smem, stream, 1u, p);
 }
 
 template <int D, typename KV>
@@ -184,6 +185,8 @@ lse_merge_kernel(void *out, int out_bf16, const float *tmp_out, const float *max
     extern __shared__ float wgt[];  // [max_partitions]
     __shared__ float s_inv;
     const int h = blockIdx.x, b = blockIdx.y;
+    grid_dependency_wait();
+    grid_dependents_launch();
     int len = context_lens[b];
     if (len < 0) len = 0;
     // partition_size 0: every partition of the row (empty ones carry a zero sum)
@@ -235,10 +238,9 @@ cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, cons
         if (e != cudaSuccess) return e;
     }
     dim3 grid(num_heads, num_seqs);
-    lse_merge_kernel<<<grid, 128, smem, stream>>>(out, out_bf16, tmp_out, max_logits, exp_sums,
-                                                  context_lens, num_heads, head_dim, max_partitions,
-                                                  partition_size);
-    return cudaGetLastError();
+    return launch_kernel(lse_merge_kernel, grid, dim3(128), smem, stream, 1u, out, out_bf16, tmp_out,
+                         max_logits, exp_sums, context_lens, num_heads, head_dim, max_partitions,
+                         partition_size);
 }
 
 }  // namespace pa

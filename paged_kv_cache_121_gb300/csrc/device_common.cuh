@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <cstdlib>
 
 namespace pa {
 
@@ -53,6 +54,55 @@ struct DecodeParams {
     int q_bf16;
     float scale_log2;    // scale * log2(e): scores are kept in base-2 units
 };
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may be scheduled while the previous kernel on the stream finishes;
+// it waits (griddepcontrol.wait) for that kernel's completion and memory
+// before reading anything, and lets its own dependents be scheduled once its
+// main work is done. Hides the launch gap between back-to-back kernels (in a
+// CUDA graph too). PA_PDL=0 launches plainly.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+inline bool pdl_enabled() {
+    static const bool v = [] {
+        const char *e = std::getenv("PA_PDL");
+        return !(e && e[0] == '0' && e[1] == 0);
+    }();
+    return v;
+}
+
+// Launch kern<<<grid, block, smem, stream>>>(args...) with programmatic
+// stream serialization (unless disabled) and, if cluster_x > 1, a cluster of
+// cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 unsigned cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // Shared-prefix pass: attention of every (sequence, query head) row over the
 // shared leading blocks, one chunk per partition, in split-K form.

@@ -58,6 +58,7 @@ prefix_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     __shared__ int s_abort;
     __shared__ int s_issued;
 
+    grid_dependency_wait();
     const int chunk = blockIdx.x;
     const int g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -230,8 +231,7 @@ cudaError_t launch_prefix_impl(const PrefixParams &p, const CUtensorMap &tk, con
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(kPrefixMaxRingBytes), done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kPrefixThreads, C::smem_bytes(p.ring_bytes), stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, dim3(kPrefixThreads), C::smem_bytes(p.ring_bytes), stream, 1u, tk, tv, p);
 }
 
 }  // namespace

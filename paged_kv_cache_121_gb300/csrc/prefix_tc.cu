@@ -97,6 +97,7 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     auto p_hi = [&](int b) { return pbuf + (2 * b) * C::kPBytes; };
     auto p_lo = [&](int b) { return pbuf + (2 * b + 1) * C::kPBytes; };
 
+    grid_dependency_wait();
     const int chunk = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tok_begin = chunk * p.chunk_tokens;
@@ -370,8 +371,7 @@ cudaError_t launch_tc_impl(const PrefixParams &p, const CUtensorMap &tk, const C
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(kTcMaxRingBytes), done);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kTcThreads, C::smem_bytes(p.ring_bytes), stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, dim3(kTcThreads), C::smem_bytes(p.ring_bytes), stream, 1u, tk, tv, p);
 }
 
 }  // namespace

@@ -521,7 +521,9 @@ def run_ours(args, rank, world, local_rank):
     achieved = alg / (decode_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     traffic = profiled_traffic(args.config) if headline else None
-    if contig:
+    if not plan["tensor_cores"]:
+        kernel = "decode_simt_kernel"
+    elif contig:
         kernel = "decode_mma_kernel<128,16> (contiguous)"
     elif bs == 8:
         kernel = "decode_mma_kernel<128,16> (two blocks per tile)"

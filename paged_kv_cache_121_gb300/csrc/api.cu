@@ -85,6 +85,7 @@ int env_int(const char *name, int lo, int hi) {
 //   PA_DECODE_RING_KB      shared-memory ring per tensor-core CTA (KiB)
 //   PA_PREFIX_KERNEL       "mma": shared-prefix pass on mma.sync (default: tcgen05)
 //   PA_PREFIX_OVERLAP      "0": shared-prefix pass not overlapped with the rest
+//   PA_DECODE_KERNEL       "simt": bf16 decode on the CUDA-core kernel
 int ctas_per_sm_override() {
     static const int v = env_int("PA_DECODE_CTAS_PER_SM", 1, 64);
     return v;
@@ -195,7 +196,18 @@ struct Plan {
     int part_tokens;    // tokens per partition
 };
 
-bool use_mma(const DecodeShape &s, bool bf16) { return bf16 && decode_mma_supported(s.head_dim, s.block_size); }
+// PA_DECODE_KERNEL=simt runs bf16 decode on the CUDA-core kernel (for comparison).
+bool simt_forced() {
+    static const bool v = [] {
+        const char *e = std::getenv("PA_DECODE_KERNEL");
+        return e && std::strcmp(e, "simt") == 0;
+    }();
+    return v;
+}
+
+bool use_mma(const DecodeShape &s, bool bf16) {
+    return bf16 && decode_mma_supported(s.head_dim, s.block_size) && !simt_forced();
+}
 
 // Partition granularity: the tensor-core kernel's tile, the CUDA-core
 // kernel's block.

@@ -527,10 +527,10 @@ def run_ours(args, rank, world, local_rank):
         kernel = "decode_mma_kernel<128,16> (contiguous)"
     elif bs == 8:
         kernel = "decode_mma_kernel<128,16> (two blocks per tile)"
-    elif bs in (16, 32, 64, 128, 256):
-        kernel = "decode_mma_kernel<128,16>"
+    elif bs < 8:
+        kernel = "decode_mma_kernel<128,16> (rows copied by cp.async, %d blocks per tile)" % (16 // bs)
     else:
-        kernel = "decode_simt_kernel"
+        kernel = "decode_mma_kernel<128,16>"
     decode_launches = plan["kernel_launches"]       # a wide split adds the merge kernel
     line = {
         "metric": ("decode attention KV GB/s, contiguous cache (unpaged baseline)" if contig
@@ -958,7 +958,7 @@ def main():
                     help="cow: decode with pa_decode_shared_prefix (the shared blocks read once)")
     ap.add_argument("--layout", choices=["paged", "contiguous"], default="paged",
                     help="contiguous: the same lengths in one reservation per sequence, no block table")
-    ap.add_argument("--block-size", type=int, default=16, choices=[4, 8, 16, 32, 64, 128],
+    ap.add_argument("--block-size", type=int, default=16, choices=[1, 2, 4, 8, 16, 32, 64, 128],
                     help="tokens per block of the paged cache (the pool keeps its token count)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

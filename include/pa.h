@@ -159,7 +159,7 @@ PA_API pa_status pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, con
  *                workspace must not overlap on the GPU.
  *   Supported: head_dim 64 or 128; num_heads % num_kv_heads == 0;
  *   (q, kv) dtypes (F32, F32) or (BF16, BF16); block_size 1..256.
- *   bf16 caches with block_size 8, 16, 32, 64, 128 or 256 run the
+ *   bf16 caches whose block_size is a power of two (1 to 256) run the
  *   tensor-core kernel, the rest the CUDA-core kernel.
  * ---------------------------------------------------------------------- */
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,

@@ -337,7 +337,7 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
         const int box = decode_mma_box_tokens(s.block_size);
         const int box_heads = p.heads_per_cta;     // one box covers every head of the CTA
         const int stage = decode_mma_stage_bytes(s.head_dim, s.block_size, p.heads_per_cta);
-        p.ring_bytes = std::max(stage, (ring_kb() * 1024) / stage * stage);
+        p.ring_bytes = decode_mma_ring_bytes(s.head_dim, s.block_size, p.heads_per_cta, ring_kb() * 1024);
         if (p.cluster_merge) {
             const int need = decode_mma_cluster_bytes(s.head_dim, p.heads_per_cta);
             if (p.ring_bytes < need) p.ring_bytes = static_cast<int>(cdiv64(need, stage) * stage);
@@ -487,7 +487,9 @@ pa_status check_prefix_call(const DecodeShape &s, pa_dtype q_dtype, pa_dtype kv_
     if (st != PA_OK) return st;
     if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
     if (shared_blocks < 0 || shared_blocks > s.max_blocks) return PA_ERR_INVALID_ARG;
-    if (kv_dtype != PA_BF16 || !decode_mma_supported(s.head_dim, s.block_size)) return PA_ERR_UNSUPPORTED;
+    // the prefix passes land one block (up to a tile) per TMA box: 8 rows or more
+    if (kv_dtype != PA_BF16 || !decode_mma_supported(s.head_dim, s.block_size) || s.block_size < 8)
+        return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 

@@ -45,7 +45,8 @@ namespace pa {
 template <int D, int TT>
 struct MmaCfg {
     static constexpr int kMaxHeads = 8;                 // KV heads per CTA = consumer warps
-    static constexpr int kThreads = 32 * (kMaxHeads + 1);
+    static constexpr int kThreads = 32 * (kMaxHeads + 1);   // one producer warp (rows mode: two)
+    __host__ __device__ static constexpr int producers(int load_mode) { return load_mode == 2 ? 2 : 1; }
     static constexpr int kHalves = D / 64;
     static constexpr int kHalfBytes = TT * 128;         // one 64-dim half of one head's tile
     static constexpr int kHeadBytes = TT * D * 2;       // one head's K (or V) rows of a tile
@@ -191,8 +192,16 @@ __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, co
     cluster_sync_all();   // peers have finished reading this CTA's shared memory
 }
 
-template <int D, int TT, bool kCluster, bool kPairs>
-__global__ void __launch_bounds__(MmaCfg<D, TT>::kThreads, 1)
+// How the producer fills a stage: one TMA box per tile (blocks of 16 tokens
+// or more), two boxes per tile (blocks of 8), or one bulk copy per token row
+// (blocks of 1, 2 or 4 tokens: a box of fewer than 8 rows cannot fill the
+// 1024-byte swizzle atom on its own). Rows mode lays a stage out as
+// [token][head][dim] with rows padded by 16 bytes instead of swizzled.
+enum LoadMode { kLoadBox = 0, kLoadPairs = 1, kLoadRows = 2 };
+static_assert(MmaCfg<128, 16>::producers(kLoadRows) == 2 && MmaCfg<128, 16>::producers(kLoadBox) == 1, "");
+
+template <int D, int TT, bool kCluster, int kLoad>
+__global__ void __launch_bounds__(32 * (MmaCfg<D, TT>::kMaxHeads + MmaCfg<D, TT>::producers(kLoad)), 1)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ DecodeParams p) {
@@ -227,27 +236,34 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tok_end = w.tok_end;
     const int ntiles = tok_end > tok_begin ? (tok_end - tok_begin + TT - 1) / TT : 0;
     const int bs = p.block_size;
-    // A tile is TT tokens of one block, or (kPairs: blocks of TT / 2 tokens)
-    // two whole blocks back to back, one TMA box of box_rows rows each. (A
-    // separate instantiation: the second box's loads, even never taken,
-    // slow the single-box loop.)
+    // A tile is TT tokens of one block; or (pairs: blocks of TT / 2 tokens)
+    // two whole blocks back to back, one TMA box of box_rows rows each; or
+    // (copies) TT / bs short blocks, gathered row by row into the one-box
+    // layout. (Separate instantiations: the second box's loads, even never
+    // taken, slow the single-box loop.)
+    constexpr bool kPairs = kLoad == kLoadPairs;
+    constexpr bool kRows = kLoad == kLoadRows;
     constexpr int bpt = kPairs ? 2 : 1;
     constexpr int box_rows = TT / bpt;
-    const int stage_bytes = 2 * hpc * C::kHeadBytes;
+    // rows mode: one token's K (or V) for the group's heads, plus 16 bytes of
+    // padding that puts 8 consecutive rows in 8 different bank groups
+    const int row_pitch = hpc * D * 2 + 16;
+    const int stage_bytes = kRows ? 2 * TT * row_pitch : 2 * hpc * C::kHeadBytes;
     int nstages = p.ring_bytes / stage_bytes;
     if (nstages > C::kMaxStages) nstages = C::kMaxStages;
-    const int v_off = hpc * C::kHeadBytes;
+    const int v_off = stage_bytes / 2;
     // byte offsets within one stage's K (or V): head, 64-dim half, token row
-    constexpr int kHalfStride = box_rows * 128;
-    constexpr int kHeadStride = C::kHalves * kHalfStride;
+    constexpr int kHalfStride = kRows ? 128 : box_rows * 128;
+    constexpr int kHeadStride = kRows ? D * 2 : C::kHalves * kHalfStride;
     const int pair_stride = hpc * kHeadStride;     // second block of a pair
     auto tok_off = [&](int t) -> int {
-        return kPairs ? (t / box_rows) * pair_stride + (t % box_rows) * 128 : t * 128;
+        return kRows ? t * row_pitch : kPairs ? (t / box_rows) * pair_stride + (t % box_rows) * 128 : t * 128;
     };
 
+    constexpr int kProducers = C::producers(kLoad);
     if (threadIdx.x == 0) {
         for (int s = 0; s < nstages; ++s) {
-            mbar_init(smem_addr(&bars[s]), 1);
+            mbar_init(smem_addr(&bars[s]), kProducers);   // one arrival per producer warp
             mbar_init(smem_addr(&bars[C::kMaxStages + s]), hpc);
         }
         s_abort = 0;
@@ -259,7 +275,73 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     WarpState<D> st;
     st.init();
 
-    if (warp == hpc) {
+    if (kRows && warp >= hpc) {
+        // ------------------------ producers (short blocks) --------------------
+        // Per tile, lane t < 16 of the first producer warp copies token t's K
+        // row, and of the second its V row (the group's heads: hpc * D * 2
+        // contiguous bytes of the cache), one bulk copy each, counted in bytes
+        // on the stage's mbarrier. (A warp issues bulk copies one at a time:
+        // two warps double the rate at which the copies start.) The block ids
+        // of 32 blocks are held one per lane and fetched a chunk ahead; a
+        // tile's TT / bs blocks never straddle two chunks (bs divides TT
+        // divides 32).
+        const bool is_v = warp > hpc;
+        const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
+        const int bs_shift = __ffs(bs) - 1;
+        const int nb = TT >> bs_shift;                                  // blocks per tile
+        const int blk_begin = tok_begin >> bs_shift;                    // tok_begin is whole tiles
+        const int nblk = (tok_end - tok_begin + bs - 1) >> bs_shift;    // blocks of this partition
+        auto entry = [&](int j) -> int { return j < nblk ? table[blk_begin + j] : 0; };
+        int cur = entry(lane), nxt = entry(32 + lane);
+        const uint64_t policy = l2_policy_evict_first();
+        const int64_t row_bytes = static_cast<int64_t>(p.num_kv_heads) * D * 2;   // one token, all heads
+        const int64_t blk_bytes = row_bytes * bs;
+        const uint32_t grp_bytes = static_cast<uint32_t>(hpc * D * 2);           // copied per row
+        const int t = lane & (TT - 1);
+        const unsigned char *src_base = static_cast<const unsigned char *>(is_v ? p.v_cache : p.k_cache) +
+                                        hgrp * hpc * D * 2 + (t & (bs - 1)) * row_bytes;
+        const uint32_t dst_lane = static_cast<uint32_t>((is_v ? v_off : 0) + t * row_pitch);
+        int issued = 0;
+        for (int i = 0; i < ntiles; ++i) {
+            const int j0 = i * nb;
+            if ((j0 & 31) == 0 && j0 > 0) {
+                cur = nxt;
+                nxt = entry(j0 + 32 + lane);
+            }
+            const int blk = __shfl_sync(0xffffffffu, cur, (j0 + (t >> bs_shift)) & 31);
+            const bool live = lane < TT && t < min(TT, tok_end - (tok_begin + i * TT));
+            // a block id outside the pool is not read: its rows are zeroed
+            const bool in_pool = static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks);
+            const unsigned ncopy = __popc(__ballot_sync(0xffffffffu, live && in_pool));
+            int ok = 1;
+            const int s = i % nstages, k = i / nstages;
+            const uint32_t full = smem_addr(&bars[s]);
+            if (lane == 0) {
+                if (k > 0) {
+                    if (*reinterpret_cast<volatile int *>(&s_abort)) {
+                        ok = 0;
+                    } else if (!mbar_wait(smem_addr(&bars[C::kMaxStages + s]), (k - 1) & 1)) {
+                        record_status(p.status, kStatusTimeout);
+                        s_abort = 1;
+                        ok = 0;
+                    }
+                }
+                if (ok) mbar_expect_tx(full, ncopy * grp_bytes);
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            const uint32_t dst = smem_addr(smem + s * stage_bytes) + dst_lane;
+            if (live && in_pool) {
+                bulk_load(dst, src_base + blk * blk_bytes, grp_bytes, full, policy);
+            } else if (live) {
+                for (uint32_t o = 0; o < grp_bytes; o += 16)
+                    *reinterpret_cast<uint4 *>(smem + s * stage_bytes + dst_lane + o) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full);   // after the zeroed rows: the phase covers them
+            issued = i + 1;
+        }
+        if (lane == 0 && !is_v) s_issued = issued;
+    } else if (!kRows && warp == hpc) {
         // ------------------------------ producer ------------------------------
         // paged: each box's block id from the table; contiguous: token offset only
         const bool contig = p.contig_stride > 0;
@@ -348,7 +430,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 s_abort = 1;
                 break;
             }
-            unsigned char *kst = smem + s * stage_bytes + warp * kHeadStride;   // this head
+            unsigned char *kst = smem + s * stage_bytes + warp * kHeadStride;   // this head (rows: its dims)
             const uint32_t kbase = smem_addr(kst);
             const uint32_t vbase = kbase + v_off;
             const int valid = min(TT, tok_end - (tok_begin + i * TT));
@@ -363,7 +445,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 __syncwarp();
             }
 
-            warp_tile_attention<D, TT>(st, qa, kbase, vbase, kHalfStride, tok_off, valid, valid, sl2, lane);
+            warp_tile_attention<D, TT, !kRows>(st, qa, kbase, vbase, kHalfStride, tok_off, valid, valid, sl2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[C::kMaxStages + s]));
         }
@@ -388,20 +470,20 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
-template <int D, int TT, bool kPairs>
+template <int D, int TT, int kLoad>
 static cudaError_t launch_impl(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                dim3 grid, cudaStream_t stream) {
     using C = MmaCfg<D, TT>;
     const size_t smem = C::smem_bytes(p.ring_bytes);
-    const dim3 block(32 * (p.heads_per_cta + 1));
+    const dim3 block(32 * (p.heads_per_cta + C::producers(kLoad)));
     if (!p.cluster_merge) {
-        auto kern = decode_mma_kernel<D, TT, false, kPairs>;
+        auto kern = decode_mma_kernel<D, TT, false, kLoad>;
         static unsigned long long done = 0;
         cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
         if (e != cudaSuccess) return e;
         return launch_kernel(kern, grid, block, smem, stream, 1u, tk, tv, p);
     }
-    auto kern = decode_mma_kernel<D, TT, true, kPairs>;
+    auto kern = decode_mma_kernel<D, TT, true, kLoad>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
     if (e != cudaSuccess) return e;
@@ -409,9 +491,8 @@ static cudaError_t launch_impl(const DecodeParams &p, const CUtensorMap &tk, con
 }
 
 bool decode_mma_supported(int head_dim, int block_size) {
-    return (head_dim == 64 || head_dim == 128) &&
-           (block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64 ||
-            block_size == 128 || block_size == 256);
+    return (head_dim == 64 || head_dim == 128) && block_size >= 1 && block_size <= 256 &&
+           (block_size & (block_size - 1)) == 0;
 }
 
 int decode_mma_tile_tokens(int) { return 16; }
@@ -425,22 +506,44 @@ int decode_mma_heads_per_cta(int num_kv_heads, int max_heads) {
 }
 
 int decode_mma_stage_bytes(int head_dim, int block_size, int heads_per_cta) {
-    return 2 * heads_per_cta * decode_mma_tile_tokens(block_size) * head_dim * 2;
+    const int tt = decode_mma_tile_tokens(block_size);
+    if (block_size < 8) return 2 * tt * (heads_per_cta * head_dim * 2 + 16);   // padded token rows
+    return 2 * heads_per_cta * tt * head_dim * 2;
+}
+
+int decode_mma_ring_bytes(int head_dim, int block_size, int heads_per_cta, int budget_bytes) {
+    // stages are counted at the unpadded size, so that the padding of rows
+    // mode does not cost a stage of the budget
+    const int stage = decode_mma_stage_bytes(head_dim, block_size, heads_per_cta);
+    const int nominal = 2 * heads_per_cta * decode_mma_tile_tokens(block_size) * head_dim * 2;
+    int n = budget_bytes / nominal;
+    while (n > 1 && n * stage > MmaCfg<128, 16>::kMaxRingBytes) --n;
+    return (n < 1 ? 1 : n) * stage;
 }
 
 int decode_mma_cluster_bytes(int head_dim, int heads_per_cta) {
     return heads_per_cta * (32 + kRowsPerTile * head_dim) * 4;
 }
 
+int decode_mma_load_mode(int block_size, bool contiguous) {
+    if (contiguous || block_size >= 16) return kLoadBox;
+    return block_size == 8 ? kLoadPairs : kLoadRows;   // blocks of 8: two per 16-token tile
+}
+
+template <int D>
+static cudaError_t launch_for_dim(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                  dim3 grid, cudaStream_t stream) {
+    switch (decode_mma_load_mode(p.block_size, p.contig_stride > 0)) {
+        case kLoadBox: return launch_impl<D, 16, kLoadBox>(p, tk, tv, grid, stream);
+        case kLoadPairs: return launch_impl<D, 16, kLoadPairs>(p, tk, tv, grid, stream);
+        default: return launch_impl<D, 16, kLoadRows>(p, tk, tv, grid, stream);
+    }
+}
+
 cudaError_t launch_decode_mma(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                               dim3 grid, cudaStream_t stream) {
-    const bool pairs = p.block_size < 16;     // blocks of 8: two per 16-token tile
-    if (p.head_dim == 128)
-        return pairs ? launch_impl<128, 16, true>(p, tk, tv, grid, stream)
-                     : launch_impl<128, 16, false>(p, tk, tv, grid, stream);
-    if (p.head_dim == 64)
-        return pairs ? launch_impl<64, 16, true>(p, tk, tv, grid, stream)
-                     : launch_impl<64, 16, false>(p, tk, tv, grid, stream);
+    if (p.head_dim == 128) return launch_for_dim<128>(p, tk, tv, grid, stream);
+    if (p.head_dim == 64) return launch_for_dim<64>(p, tk, tv, grid, stream);
     return cudaErrorInvalidValue;
 }
 

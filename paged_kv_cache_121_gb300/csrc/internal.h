@@ -10,11 +10,12 @@ namespace pa {
 struct DecodeParams;
 struct PrefixParams;
 
-bool decode_mma_supported(int head_dim, int block_size);
+bool decode_mma_supported(int head_dim, int block_size);   // D 64/128, blocks of 1..256 (powers of two)
 int decode_mma_tile_tokens(int block_size);       // tokens per pipeline stage (16)
 int decode_mma_box_tokens(int block_size);        // rows per TMA box: min(block_size, 16)
 int decode_mma_heads_per_cta(int num_kv_heads, int max_heads);   // KV heads (consumer warps) per CTA
 int decode_mma_stage_bytes(int head_dim, int block_size, int heads_per_cta);
+int decode_mma_ring_bytes(int head_dim, int block_size, int heads_per_cta, int budget_bytes);   // whole stages
 int decode_mma_cluster_bytes(int head_dim, int heads_per_cta);   // shared memory the cluster merge needs
 constexpr int kMaxClusterSplits = 8;                              // portable cluster size
 cudaError_t launch_decode_mma(const DecodeParams &p, const CUtensorMap &tmap_k,

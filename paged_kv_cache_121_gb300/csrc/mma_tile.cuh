@@ -4,10 +4,11 @@
 // Optimize?", section 8: softmax(scale q K^T) V, computed block by block).
 // Shared by the paged decode kernel and the shared-prefix kernel.
 //
-// Shared-memory tile layout (written by TMA with the 128-byte swizzle): for
-// each 64-dim half of the head dimension, 16 token rows of 128 bytes; row t
-// of half c lives at base + c * half_stride + tok_off(t), and its 16-byte
-// chunk j is stored at chunk j ^ (t & 7).
+// Shared-memory tile layout: for each 64-dim half of the head dimension, 16
+// token rows of 128 bytes; row t of half c lives at base + c * half_stride +
+// tok_off(t). Swizzled (written by TMA with the 128-byte swizzle): its
+// 16-byte chunk j is stored at chunk j ^ (t & 7). Unswizzled: at chunk j,
+// with row starts spread over the banks by the caller's tok_off.
 #pragma once
 
 #include "device_common.cuh"
@@ -67,7 +68,7 @@ __device__ __forceinline__ void load_query_fragments(uint32_t (&qa)[D / 16][4], 
 // S = Q K^T for the tile, masking, online softmax update, O += P V. Tokens at
 // or past valid0 (row r) / valid1 (row r + 8) get score -inf. V rows of tokens
 // past the tile's data must already hold zeros (0 * NaN would leak).
-template <int D, int TT, typename TokOff>
+template <int D, int TT, bool kSwizzled = true, typename TokOff>
 __device__ __forceinline__ void warp_tile_attention(WarpState<D> &st, const uint32_t (&qa)[D / 16][4],
                                                     uint32_t kbase, uint32_t vbase, int half_stride,
                                                     TokOff tok_off, int valid0, int valid1, float sl2,
@@ -86,7 +87,8 @@ __device__ __forceinline__ void warp_tile_attention(WarpState<D> &st, const uint
         for (int kk = 0; kk < D / 16; kk += 2) {
             const int tok = 8 * j + (lane & 7);
             const int c = 2 * kk + (lane >> 3);
-            const uint32_t addr = kbase + (c >> 3) * half_stride + tok_off(tok) + (((c & 7) ^ (tok & 7)) << 4);
+            const uint32_t addr = kbase + (c >> 3) * half_stride + tok_off(tok) +
+                                  (((c & 7) ^ (kSwizzled ? tok & 7 : 0)) << 4);
             uint32_t b0, b1, b2, b3;
             ldmatrix_x4(addr, b0, b1, b2, b3);
             mma_bf16_16816(sacc[j], qa[kk], b0, b1);
@@ -157,7 +159,8 @@ __device__ __forceinline__ void warp_tile_attention(WarpState<D> &st, const uint
         const int mi = lane >> 3;
         const int tok = (mi & 1) * 8 + (lane & 7);
         const int c = dn + (mi >> 1);
-        const uint32_t addr = vbase + (c >> 3) * half_stride + tok_off(tok) + (((c & 7) ^ (tok & 7)) << 4);
+        const uint32_t addr = vbase + (c >> 3) * half_stride + tok_off(tok) +
+                              (((c & 7) ^ (kSwizzled ? tok & 7 : 0)) << 4);
         uint32_t v0, v1, v2, v3;
         ldmatrix_x4_trans(addr, v0, v1, v2, v3);
         mma_bf16_16816(st.o[dn], phi, v0, v1);

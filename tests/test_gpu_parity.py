@@ -35,7 +35,12 @@ SMALL = [
     ((5, 40, 129), 4, 4, 64, 16, True),            # G = 1
     ((3, 77, 300), 16, 1, 64, 32, True),           # G = 16, one full tile of heads
     ((50, 260), 64, 2, 128, 16, True),             # G = 32: two head tiles
-    ((19, 90), 8, 2, 128, 4, True),                # block size outside the tensor-core set
+    ((19, 90), 8, 2, 128, 4, True),                # blocks of 4: rows gathered by 16-byte copies
+    ((1, 3, 16, 17, 95, 400), 16, 4, 128, 1, True),  # blocks of 1: 16 table entries per tile
+    ((2, 33, 64, 250), 8, 8, 64, 2, True),         # blocks of 2, G = 1
+    ((9, 700), 24, 12, 128, 4, True),              # blocks of 4, groups of 6 heads, split
+    ((7, 130), 4, 1, 64, 4, True),                 # one KV head: 8 chunks per token row
+    ((12, 40), 8, 2, 128, 12, True),               # block size not a power of two: CUDA-core kernel
     ((19, 90), 8, 2, 64, 64, True),
     ((10, 45), 6, 3, 64, 16, False),
     ((33, 200, 17), 24, 12, 128, 16, True),        # 12 KV heads: groups of 6 per CTA
@@ -67,13 +72,14 @@ def test_decode_small(case, use_ws):
     assert_clean_status()
 
 
-@pytest.mark.parametrize("bs", [16, 8])
+@pytest.mark.parametrize("bs", [16, 8, 4, 1])
 def test_decode_nan_in_unused_slots_and_table_tail(bs):
     """Slots past a context and table entries past its blocks hold garbage:
     neither may reach the output (blocks of 8: a 16-token tile whose second
     block lies past the context must not read that block's table entry)."""
     lens, Hq, Hkv, D = (5, 17, 40), 8, 2, 128
-    batch = workloads.make_batch("nan", lens, Hq, Hkv, D, bs, 32, True, seed_values=7)
+    pool = sum(workloads.cdiv(n, bs) for n in lens) + 8
+    batch = workloads.make_batch("nan", lens, Hq, Hkv, D, bs, pool, True, seed_values=7)
     k, v = batch.k_cache, batch.v_cache
     for b, n in enumerate(lens):
         last = batch.block_tables[b, workloads.cdiv(n, bs) - 1]
@@ -127,7 +133,7 @@ def test_decode_bf16_output():
 # ---------------------------------------------------------------------------
 # split-K partitions and the log-sum-exp merge
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("bs,ps", [(16, 512), (8, 64), (32, 96), (16, 48), (8, 24)])
+@pytest.mark.parametrize("bs,ps", [(16, 512), (8, 64), (32, 96), (16, 48), (8, 24), (4, 32), (1, 48)])
 def test_splitk_partitions_and_merge(bs, ps):
     lens = (1, 100, 511, 512, 513, 1500)
     Hq, Hkv, D = 16, 4, 128
@@ -238,7 +244,7 @@ def test_qwen3_workload():
     assert_clean_status()
 
 
-@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("bs", [4, 8, 16, 32])
 def test_long_context_workload(bs):
     batch = workloads.long_context(block_size=bs)
     db = DeviceBatch(batch)

@@ -14,7 +14,9 @@ SHAPES = [
     (64, 32, 8, 128, 16, 4096),     # GQA batch
     (16, 32, 8, 128, 8, 4164),
     (16, 32, 8, 128, 128, 4164),
-    (3, 8, 2, 64, 4, 500),          # blocks of 4: CUDA-core kernel
+    (3, 8, 2, 64, 4, 500),          # blocks of 4: tensor cores, rows copied by cp.async
+    (16, 32, 8, 128, 1, 4164),      # blocks of 1
+    (3, 8, 2, 64, 12, 500),         # block size not a power of two: CUDA-core kernel
     (1, 8, 8, 128, 16, 1),
 ]
 
@@ -24,7 +26,7 @@ SHAPES = [
 def test_plan_is_consistent(shape, with_ws):
     B, hq, hkv, d, bs, mcl = shape
     p = pa.pa_decode_plan(B, hq, hkv, d, bs, mcl, pa.PA_BF16, with_workspace=with_ws)
-    assert p["tensor_cores"] == (1 if bs >= 8 else 0)
+    assert p["tensor_cores"] == (1 if bs & (bs - 1) == 0 else 0)
     assert hkv % p["heads_per_cta"] == 0
     assert p["num_splits"] >= 1
     # the partitions cover the context, and none is empty by construction

@@ -120,7 +120,7 @@ def measured_peaks():
 
 def decode_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("decode_mma.cu", "device_common.cuh"):
+    for f in ("decode_mma.cu", "device_common.cuh", "mma_tile.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_121_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -66,7 +66,7 @@ typedef enum pa_dtype {
 PA_API const char *pa_status_string(pa_status status);
 
 /* ABI version of this header (increases on any incompatible change). */
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 PA_API int pa_abi_version(void);
 
 /* ------------------------------------------------------------------------
@@ -161,6 +161,14 @@ PA_API pa_status pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, con
  *   (q, kv) dtypes (F32, F32) or (BF16, BF16); block_size 1..256.
  *   bf16 caches whose block_size is a power of two (1 to 256) run the
  *   tensor-core kernel, the rest the CUDA-core kernel.
+ *   Ragged batches: with a workspace, blocks of 16 or more and so many
+ *   sequences (2 to 2,048) that the per-partition plan would cut each
+ *   context at most twice, the tensor-core path cuts the whole batch's
+ *   16-token tiles, sequence after sequence, into equal ranges per CTA on
+ *   the device (where the lengths are) and merges the pieces of sequences
+ *   that straddle two ranges: every CTA gets the same work however ragged
+ *   the lengths. PA_DECODE_BALANCE=0 / 1 turns it off / on wherever it
+ *   applies.
  * ---------------------------------------------------------------------- */
 PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                        int head_dim, int block_size, int max_context_len);
@@ -177,6 +185,8 @@ typedef struct pa_decode_plan_t {
     int cluster_merge;      /* 1: partitions merged inside a thread-block cluster */
     int kernel_launches;    /* kernels one call launches: 1, or 2 (decode + merge) */
     size_t workspace_bytes; /* workspace the plan uses (0: none) */
+    int balanced;           /* 1: ragged-balanced decode (num_splits = CTAs per KV-head
+                               group, partition_tokens 0: ranges are cut on the device) */
 } pa_decode_plan_t;
 
 PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim,

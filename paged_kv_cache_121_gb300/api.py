@@ -94,7 +94,7 @@ class DecodePlan(ctypes.Structure):
     _fields_ = [("tensor_cores", ctypes.c_int), ("heads_per_cta", ctypes.c_int),
                 ("num_splits", ctypes.c_int), ("partition_tokens", ctypes.c_int),
                 ("cluster_merge", ctypes.c_int), ("kernel_launches", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("balanced", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: int(getattr(self, name)) for name, _ in self._fields_}

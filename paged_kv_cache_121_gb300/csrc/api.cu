@@ -86,6 +86,7 @@ int env_int(const char *name, int lo, int hi) {
 //   PA_PREFIX_KERNEL       "mma": shared-prefix pass on mma.sync (default: tcgen05)
 //   PA_PREFIX_OVERLAP      "0": shared-prefix pass not overlapped with the rest
 //   PA_DECODE_KERNEL       "simt": bf16 decode on the CUDA-core kernel
+//   PA_DECODE_BALANCE      "0": never the ragged-balanced decode, "1": whenever it applies
 int ctas_per_sm_override() {
     static const int v = env_int("PA_DECODE_CTAS_PER_SM", 1, 64);
     return v;
@@ -125,6 +126,16 @@ bool prefix_tc_enabled() {
     }();
     return v;
 }
+// PA_DECODE_BALANCE: -1 automatic (default), 0 never, 1 whenever it applies.
+int balance_mode() {
+    static const int v = [] {
+        const char *e = std::getenv("PA_DECODE_BALANCE");
+        if (!e) return -1;
+        return std::strcmp(e, "0") == 0 ? 0 : std::strcmp(e, "1") == 0 ? 1 : -1;
+    }();
+    return v;
+}
+
 int ring_kb() {
     static const int v = env_int("PA_DECODE_RING_KB", 16, 200);
     return v ? v : kMmaRingKiB;
@@ -194,6 +205,8 @@ struct Plan {
     int ntile;
     int nsplit;
     int part_tokens;    // tokens per partition
+    bool balanced = false;   // ragged-balanced decode: the batch's tiles cut into equal ranges
+    int bal_ctas = 0;        //   CTAs per (KV-head group, head tile)
 };
 
 // PA_DECODE_KERNEL=simt runs bf16 decode on the CUDA-core kernel (for comparison).
@@ -259,8 +272,36 @@ Plan plan_split(const DecodeShape &s, int sms, bool mma, int min_split_tokens = 
 
 // The plan pa_decode uses: with no workspace, a split the tensor-core kernel
 // cannot keep inside a cluster is trimmed to one (CUDA-core: not split).
-Plan plan_decode(const DecodeShape &s, int sms, bool mma, bool have_workspace) {
+// The ragged-balanced decode applies to a paged bf16 cache with blocks of 16
+// or more, a workspace, and a batch whose tile count fits an int. By default
+// it is taken when the batch has so many sequences that the CTA slots would
+// split each context at most twice: there, ragged lengths leave the CTAs of
+// long contexts running alone.
+bool take_balanced(const DecodeShape &s, const Plan &pl, int sms, bool have_workspace, bool paged) {
+    if (!pl.mma || !have_workspace || !paged || s.num_seqs < 1 || s.num_seqs > kBalancedMaxSeqs) return false;
+    if (!decode_balanced_supported(s.head_dim, s.block_size)) return false;
+    if (static_cast<int64_t>(s.num_seqs) * cdiv64(s.max_ctx, 16) >= (int64_t(1) << 30)) return false;
+    const int mode = balance_mode();
+    if (mode >= 0) return mode == 1;
+    // enough sequences that the CTA slots would split each context at most twice
+    const int64_t units = static_cast<int64_t>(s.num_seqs) * (s.num_kv_heads / pl.heads_per_cta) * pl.ntile;
+    const int per_sm = ctas_per_sm_override() ? ctas_per_sm_override() : kCtasPerSmMma;
+    return s.num_seqs >= 2 && units * 3 > static_cast<int64_t>(sms) * per_sm;
+}
+
+Plan plan_decode(const DecodeShape &s, int sms, bool mma, bool have_workspace, bool paged = true) {
     Plan pl = plan_split(s, sms, mma);
+    pl.balanced = take_balanced(s, pl, sms, have_workspace, paged);
+    pl.bal_ctas = 0;
+    if (pl.balanced) {
+        const int lanes = (s.num_kv_heads / pl.heads_per_cta) * pl.ntile;
+        const int per_sm = ctas_per_sm_override() ? ctas_per_sm_override() : kCtasPerSmMma;
+        pl.bal_ctas = std::max(1, sms * per_sm / lanes);
+        pl.cluster = false;
+        pl.nsplit = pl.bal_ctas;
+        pl.part_tokens = 0;
+        return pl;
+    }
     if (!have_workspace && !pl.cluster) {
         const int gran = split_granule(s, mma);
         const int64_t ngran = std::max<int64_t>(1, cdiv64(s.max_ctx, gran));
@@ -278,13 +319,23 @@ Plan plan_decode(const DecodeShape &s, int sms, bool mma, bool have_workspace) {
 }
 
 struct WorkspaceLayout {
-    size_t o_off, ml_off, count_off, total;
+    size_t o_off, ml_off, count_off, prefix_off, total;
 };
 
 // Wide splits are written in split-K form (normalised partial outputs,
 // maxima, sums) and merged by the log-sum-exp merge kernel.
 WorkspaceLayout workspace_layout(const DecodeShape &s, const Plan &pl) {
     WorkspaceLayout w{};
+    if (pl.balanced) {
+        // pieces: rows (c + b) * Hq + h for c < ctas, b < num_seqs; then the tile prefix sums
+        const size_t rows = static_cast<size_t>(pl.bal_ctas + s.num_seqs) * s.num_heads;
+        w.o_off = 0;
+        w.ml_off = align256(rows * s.head_dim * sizeof(float));
+        w.count_off = w.ml_off + align256(rows * sizeof(float));
+        w.prefix_off = w.count_off + align256(rows * sizeof(float));
+        w.total = w.prefix_off + align256(static_cast<size_t>(s.num_seqs + 1) * sizeof(int));
+        return w;
+    }
     if (pl.nsplit <= 1 || pl.cluster) return w;
     const size_t rows = static_cast<size_t>(s.num_seqs) * s.num_heads * pl.nsplit;
     w.o_off = 0;
@@ -358,6 +409,39 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// Ragged-balanced decode: equal tile ranges per CTA, then the merge of the
+// pieces of sequences split between CTAs (both through the workspace).
+pa_status launch_balanced(const DecodeShape &s, DecodeParams &p, const Plan &pl, int dev, void *workspace,
+                          const WorkspaceLayout &wl, cudaStream_t stream) {
+    p.status = status_word(dev);
+    if (!p.status) return PA_ERR_CUDA;
+    char *ws = static_cast<char *>(workspace);
+    p.tmp_out = reinterpret_cast<float *>(ws + wl.o_off);
+    p.max_logits = reinterpret_cast<float *>(ws + wl.ml_off);
+    p.exp_sums = reinterpret_cast<float *>(ws + wl.count_off);
+    p.mode = kModeSplitK;
+    p.cluster_merge = 0;
+    BalancedParams bp;
+    bp.ctas = pl.bal_ctas;
+    bp.len_cap = s.max_ctx;
+    bp.prefix = reinterpret_cast<int *>(ws + wl.prefix_off);
+    const int stage = decode_mma_stage_bytes(s.head_dim, s.block_size, p.heads_per_cta);
+    p.ring_bytes = decode_mma_ring_bytes(s.head_dim, s.block_size, p.heads_per_cta, ring_kb() * 1024);
+    if (p.ring_bytes < stage) return PA_ERR_UNSUPPORTED;
+    const int box = decode_mma_box_tokens(s.block_size);
+    CUtensorMap tk, tv;
+    pa_status st = make_cache_map(&tk, p.k_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim, box,
+                                  p.heads_per_cta);
+    if (st != PA_OK) return st;
+    if ((st = make_cache_map(&tv, p.v_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim, box,
+                             p.heads_per_cta)) != PA_OK)
+        return st;
+    const dim3 grid(static_cast<unsigned>(pl.bal_ctas),
+                    static_cast<unsigned>((s.num_kv_heads / p.heads_per_cta) * p.ntile), 1u);
+    if (launch_decode_balanced(p, bp, tk, tv, grid, stream) != cudaSuccess) return PA_ERR_CUDA;
+    return launch_balanced_merge(p, bp, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 void fill_common(DecodeParams &p, const DecodeShape &s, const void *query, pa_dtype q_dtype,
                  const void *k_cache, const void *v_cache, const int32_t *block_tables,
                  const int32_t *context_lens, float scale) {
@@ -396,7 +480,7 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
     if (sms <= 0) return PA_ERR_CUDA;
 
     const Plan pl = plan_decode(s, sms, use_mma(s, kv_dtype == PA_BF16),
-                                workspace != nullptr || workspace_bytes != 0);
+                                workspace != nullptr || workspace_bytes != 0, contig_stride == 0);
     DecodeParams p;
     fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
     p.contig_stride = contig_stride;
@@ -407,6 +491,11 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
     p.nsplit = pl.nsplit;
     p.part_tokens = pl.part_tokens;
     p.cluster_merge = pl.cluster ? 1 : 0;
+    if (pl.balanced) {
+        const WorkspaceLayout wl = workspace_layout(s, pl);
+        if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+        return launch_balanced(s, p, pl, dev, workspace, wl, as_stream(stream));
+    }
     if (pl.cluster) {
         p.mode = kModeFinal;   // the cluster merge writes the output
     } else if (pl.nsplit > 1) {
@@ -639,8 +728,9 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_h
     if (current_device(&dev) != PA_OK) return 0;
     const int sms = sm_count(dev);
     if (sms <= 0) return 0;
-    return std::max(workspace_layout(s, plan_split(s, sms, true)).total,
-                    workspace_layout(s, plan_split(s, sms, false)).total);
+    return std::max({workspace_layout(s, plan_split(s, sms, true)).total,
+                     workspace_layout(s, plan_split(s, sms, false)).total,
+                     workspace_layout(s, plan_decode(s, sms, true, true)).total});
 }
 
 PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
@@ -665,6 +755,7 @@ PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, i
     plan->cluster_merge = pl.cluster ? 1 : 0;
     plan->kernel_launches = num_seqs == 0 ? 0 : (wide ? 2 : 1);
     plan->workspace_bytes = wide ? workspace_layout(s, pl).total : 0;
+    plan->balanced = pl.balanced ? 1 : 0;
     return PA_OK;
 }
 
@@ -698,7 +789,8 @@ PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads
     const int sms = sm_count(dev);
     if (sms <= 0) return 0;
     const PrefixPlan pp = plan_prefix(s, shared_blocks, sms, prefix_tc_enabled());
-    const size_t plain = workspace_layout(s, plan_split(s, sms, true)).total;
+    const size_t plain = std::max(workspace_layout(s, plan_split(s, sms, true)).total,
+                                  workspace_layout(s, plan_decode(s, sms, true, true)).total);
     return std::max(prefix_workspace(s, pp).total, plain);
 }
 

@@ -34,6 +34,20 @@ int prefix_tc_tile_tokens();
 int prefix_tc_stage_bytes(int head_dim);
 cudaError_t launch_prefix_tc(const PrefixParams &p, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                              dim3 grid, cudaStream_t stream);
+// Balanced decode (decode_balanced.cu): the batch's tiles, concatenated
+// sequence after sequence, cut into `ctas` equal ranges per (KV-head group,
+// head tile); pieces of a sequence split between CTAs are merged after.
+struct BalancedParams {
+    int ctas;       // CTAs per (KV-head group, head tile): grid.x
+    int len_cap;    // tokens past this are not attended (max_context_len)
+    int *prefix;    // [num_seqs + 1] tile prefix sums, written by the decode for the merge
+};
+constexpr int kBalancedMaxSeqs = 2048;   // the prefix sums live in shared memory
+bool decode_balanced_supported(int head_dim, int block_size);
+size_t decode_balanced_smem_extra(int num_seqs);
+cudaError_t launch_decode_balanced(const DecodeParams &p, const BalancedParams &bp, const CUtensorMap &tmap_k,
+                                   const CUtensorMap &tmap_v, dim3 grid, cudaStream_t stream);
+cudaError_t launch_balanced_merge(const DecodeParams &p, const BalancedParams &bp, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, cudaStream_t stream);
 cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
                              const float *exp_sums, const int32_t *context_lens, int num_seqs,

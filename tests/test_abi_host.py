@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings_and_version():
     lib = _lib.load()
-    assert lib.pa_abi_version() == 1
+    assert lib.pa_abi_version() == 2
     for code in range(8):
         assert lib.pa_status_string(code)
     assert lib.pa_status_string(99) == b"unknown status"

@@ -29,6 +29,12 @@ def test_plan_is_consistent(shape, with_ws):
     assert p["tensor_cores"] == (1 if bs & (bs - 1) == 0 else 0)
     assert hkv % p["heads_per_cta"] == 0
     assert p["num_splits"] >= 1
+    if p["balanced"]:
+        # equal tile ranges cut on the device: decode + merge through the workspace
+        assert with_ws and p["tensor_cores"] and bs >= 16 and not p["cluster_merge"]
+        assert p["partition_tokens"] == 0 and p["kernel_launches"] == 2
+        assert 0 < p["workspace_bytes"] <= pa.pa_decode_workspace_size(B, hq, hkv, d, bs, mcl)
+        return
     # the partitions cover the context, and none is empty by construction
     assert p["num_splits"] * p["partition_tokens"] >= mcl
     assert (p["num_splits"] - 1) * p["partition_tokens"] < max(mcl, 1) or p["cluster_merge"]

@@ -29,6 +29,9 @@ constexpr int kCtasPerSmSimt = 2;     //   (tensor-core / CUDA-core kernel)
 constexpr int kMmaHeadsPerCta = 4;    // KV heads per tensor-core CTA (consumer warps)
 constexpr int kContiguousTile = 16;   // tokens per tile of a contiguous cache
 constexpr int kMmaRingKiB = 96;       // shared-memory ring per tensor-core CTA
+constexpr int kBalancedHeadsPerCta = 8;   // ragged-balanced decode: every KV head of a group in one CTA,
+constexpr int kBalancedCtasPerSm = 1;     //   one CTA per SM,
+constexpr int kBalancedRingKiB = 200;     //   three 64 KiB stages
 constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
 constexpr int kMinPrefixChunk = 64;   // tokens per chunk of the shared-prefix pass, at least
 constexpr int kMinRestSplitTokens = 64;   // partitions of the rest of a shared-prefix context, at least
@@ -91,10 +94,11 @@ int ctas_per_sm_override() {
     static const int v = env_int("PA_DECODE_CTAS_PER_SM", 1, 64);
     return v;
 }
-int heads_cap() {
+int heads_override() {
     static const int v = env_int("PA_DECODE_HEADS", 1, 8);
-    return v ? v : kMmaHeadsPerCta;
+    return v;
 }
+int heads_cap() { return heads_override() ? heads_override() : kMmaHeadsPerCta; }
 // PA_PREFIX_OVERLAP=0 runs the shared-prefix pass and the rest-of-context
 // decode one after the other on the caller's stream instead of side by side.
 bool prefix_overlap_enabled() {
@@ -136,10 +140,11 @@ int balance_mode() {
     return v;
 }
 
-int ring_kb() {
+int ring_override_kb() {
     static const int v = env_int("PA_DECODE_RING_KB", 16, 200);
-    return v ? v : kMmaRingKiB;
+    return v;
 }
+int ring_kb() { return ring_override_kb() ? ring_override_kb() : kMmaRingKiB; }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -294,8 +299,11 @@ Plan plan_decode(const DecodeShape &s, int sms, bool mma, bool have_workspace, b
     pl.balanced = take_balanced(s, pl, sms, have_workspace, paged);
     pl.bal_ctas = 0;
     if (pl.balanced) {
+        // whole head groups per CTA: fewer, larger boxes and one query load per head group
+        pl.heads_per_cta = decode_mma_heads_per_cta(
+            s.num_kv_heads, heads_override() ? heads_override() : kBalancedHeadsPerCta);
         const int lanes = (s.num_kv_heads / pl.heads_per_cta) * pl.ntile;
-        const int per_sm = ctas_per_sm_override() ? ctas_per_sm_override() : kCtasPerSmMma;
+        const int per_sm = ctas_per_sm_override() ? ctas_per_sm_override() : kBalancedCtasPerSm;
         pl.bal_ctas = std::max(1, sms * per_sm / lanes);
         pl.cluster = false;
         pl.nsplit = pl.bal_ctas;
@@ -426,7 +434,8 @@ pa_status launch_balanced(const DecodeShape &s, DecodeParams &p, const Plan &pl,
     bp.len_cap = s.max_ctx;
     bp.prefix = reinterpret_cast<int *>(ws + wl.prefix_off);
     const int stage = decode_mma_stage_bytes(s.head_dim, s.block_size, p.heads_per_cta);
-    p.ring_bytes = decode_mma_ring_bytes(s.head_dim, s.block_size, p.heads_per_cta, ring_kb() * 1024);
+    const int ring_budget = (ring_override_kb() ? ring_override_kb() : kBalancedRingKiB) * 1024;
+    p.ring_bytes = decode_mma_ring_bytes(s.head_dim, s.block_size, p.heads_per_cta, ring_budget);
     if (p.ring_bytes < stage) return PA_ERR_UNSUPPORTED;
     const int box = decode_mma_box_tokens(s.block_size);
     CUtensorMap tk, tv;

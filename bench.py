@@ -56,6 +56,8 @@ def build_workload(config: str, rank: int, copies: int, block_size: int = 16, la
             lens, hq, L = [workloads.QWEN3_TOKENS] * (nb * copies), 32, workloads.QWEN3_TOKENS
         elif config == "long":
             lens, hq, L = [workloads.LONG_TOKENS] * (nb * copies), 64, workloads.LONG_TOKENS
+        elif config == "gqa_uniform":
+            lens, hq, L = [workloads.GQA_UNIFORM_TOKENS] * (nb * copies), 32, workloads.GQA_UNIFORM_TOKENS
         else:
             lens, hq, L = workloads.gqa_lengths(nb * copies), 32, 4096
         desc = "%s, contiguous cache: %d seqs x %d reserved rows (lengths as the paged workload), Hq %d, Hkv 8, D 128, bf16" % (
@@ -68,6 +70,10 @@ def build_workload(config: str, rank: int, copies: int, block_size: int = 16, la
     if config == "long":
         return workloads.long_context(block_size=block_size, num_seqs=4, copies=copies), \
             "long context: 4 seqs x 32768 tokens, Hq 64, Hkv 8, D 128, bf16, block %d" % block_size
+    if config == "gqa_uniform":
+        return workloads.gqa_uniform(num_seqs=64 * copies, num_blocks=20000 * copies * 16 // block_size,
+                                     block_size=block_size), \
+            "llama gqa, uniform: 64 seqs x 2304 tokens, Hq 32, Hkv 8, D 128, bf16, block %d" % block_size
     if config == "gqa":
         return workloads.gqa(num_seqs=64 * copies, num_blocks=20000 * copies * 16 // block_size,
                              block_size=block_size), \
@@ -76,7 +82,7 @@ def build_workload(config: str, rank: int, copies: int, block_size: int = 16, la
 
 
 def per_batch(config: str) -> int:
-    return {"qwen3": 16, "long": 4, "gqa": 64}[config]
+    return {"qwen3": 16, "long": 4, "gqa": 64, "gqa_uniform": 64}[config]
 
 
 def kv_bytes(lens, hkv, d, elem) -> int:
@@ -118,15 +124,19 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_source_sha() -> str:
+DECODE_SOURCES = ("decode_mma.cu", "device_common.cuh", "mma_tile.cuh")
+BALANCED_SOURCES = ("decode_balanced.cu", "device_common.cuh", "mma_tile.cuh")
+
+
+def decode_source_sha(files=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in ("decode_mma.cu", "device_common.cuh", "mma_tile.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_cache_121_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config: str):
+def profiled_traffic(config: str, files=DECODE_SOURCES):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", f"pa_decode_{config}.md")
@@ -136,7 +146,7 @@ def profiled_traffic(config: str):
         return None
     m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != decode_source_sha():
+    if not m_sha or not m_tr or m_sha.group(1) != decode_source_sha(files):
         return None
     return float(m_tr.group(1))
 
@@ -520,7 +530,8 @@ def run_ours(args, rank, world, local_rank):
     alg = np.mean([decode_alg_bytes(v["lens_h"], hq, hkv, d, bs, elem) for v in views])
     achieved = alg / (decode_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    traffic = profiled_traffic(args.config) if headline else None
+    traffic = profiled_traffic(args.config, BALANCED_SOURCES if plan.get("balanced") else DECODE_SOURCES) \
+        if headline else None
     if not plan["tensor_cores"]:
         kernel = "decode_simt_kernel"
     elif contig:
@@ -528,13 +539,16 @@ def run_ours(args, rank, world, local_rank):
     elif bs == 8:
         kernel = "decode_mma_kernel<128,16> (two blocks per tile)"
     elif bs < 8:
-        kernel = "decode_mma_kernel<128,16> (rows copied by cp.async, %d blocks per tile)" % (16 // bs)
+        kernel = "decode_mma_kernel<128,16> (one bulk copy per token row, %d blocks per tile)" % (16 // bs)
+    elif plan.get("balanced"):
+        kernel = "decode_balanced_kernel<128> (equal tile ranges per CTA) + balanced_merge_kernel<128>"
     else:
         kernel = "decode_mma_kernel<128,16>"
     decode_launches = plan["kernel_launches"]       # a wide split adds the merge kernel
     line = {
         "metric": ("decode attention KV GB/s, contiguous cache (unpaged baseline)" if contig
-                   else "paged decode attention KV GB/s (Qwen3-8B shape)"),
+                   else "paged decode attention KV GB/s (Qwen3-8B shape)" if args.config == "qwen3"
+                   else "paged decode attention KV GB/s (%s workload)" % args.config),
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps_timed, "warmup": W,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16",
@@ -951,7 +965,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=["qwen3", "long", "gqa", "cow", "swap"], default="qwen3")
+    ap.add_argument("--config", choices=["qwen3", "long", "gqa", "gqa_uniform", "cow", "swap"], default="qwen3")
     ap.add_argument("--copies", type=int, default=0,
                     help="cow: disjoint copies of the workload held on the device (default %d)" % COW_COPIES)
     ap.add_argument("--prefix-aware", action="store_true",

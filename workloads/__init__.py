@@ -231,6 +231,16 @@ def gqa(num_seqs: int = 64, num_blocks: int = 20000, block_size: int = 16) -> De
     return make_batch("gqa", gqa_lengths(num_seqs), 32, 8, 128, block_size, num_blocks, bf16=True)
 
 
+GQA_UNIFORM_TOKENS = 2304    # the mean of U[512, 4096]: the same KV bytes as the ragged batch
+
+
+def gqa_uniform(num_seqs: int = 64, num_blocks: int = 20000, block_size: int = 16) -> DecodeBatch:
+    """The GQA batch with every length at the mean of U[512, 4096] (2,304
+    tokens): the uniform counterpart of the ragged batch."""
+    lens = np.full(num_seqs, GQA_UNIFORM_TOKENS, dtype=np.int32)
+    return make_batch("gqa_uniform", lens, 32, 8, 128, block_size, num_blocks, bf16=True)
+
+
 QWEN3_TOKENS = 4164          # 4,100-token prompt + 64 generated
 QWEN3_POOL_BLOCKS = 38348    # 613,568 cache tokens / 16
 

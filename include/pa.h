@@ -57,9 +57,13 @@ typedef enum pa_status {
     PA_ERR_NOT_FOUND = 7      /* block manager: unknown sequence id */
 } pa_status;
 
+/* Element types. The KV-size estimate of [P4] section 2 counts fp16 and bf16
+ * alike, two bytes a value; both run the same tensor-core kernels here, fp32
+ * the CUDA-core one. */
 typedef enum pa_dtype {
     PA_F32 = 0,
-    PA_BF16 = 1
+    PA_BF16 = 1,
+    PA_F16 = 2
 } pa_dtype;
 
 /* Human-readable text of a status code (static storage, never NULL). */
@@ -142,7 +146,7 @@ PA_API pa_status pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, con
  * Grouped-query attention: query head h reads KV head h / (num_heads /
  * num_kv_heads) ([P3], legend of the KV-size formula).
  *
- *   out          [num_seqs, num_heads, head_dim], out_dtype (F32 or BF16)
+ *   out          [num_seqs, num_heads, head_dim], out_dtype (F32, BF16 or F16)
  *   query        [num_seqs, num_heads, head_dim], q_dtype
  *   context_lens [num_seqs] int32: tokens attended by each sequence (the
  *                token written this step included). 0 gives an all-zero row.
@@ -158,9 +162,9 @@ PA_API pa_status pa_swap_blocks(void *dst_k, void *dst_v, const void *src_k, con
  *                contents need no initialisation. Calls that share a
  *                workspace must not overlap on the GPU.
  *   Supported: head_dim 64 or 128; num_heads % num_kv_heads == 0;
- *   (q, kv) dtypes (F32, F32) or (BF16, BF16); block_size 1..256.
- *   bf16 caches whose block_size is a power of two (1 to 256) run the
- *   tensor-core kernel, the rest the CUDA-core kernel.
+ *   (q, kv) dtypes (F32, F32), (BF16, BF16) or (F16, F16); block_size
+ *   1..256. bf16 and fp16 caches whose block_size is a power of two (1 to
+ *   256) run the tensor-core kernel, the rest the CUDA-core kernel.
  *   Ragged batches: with a workspace, blocks of 16 or more and so many
  *   sequences (2 to 2,048) that the per-partition plan would cut each
  *   context at most twice, the tensor-core path cuts the whole batch's
@@ -222,7 +226,7 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
  *   workspace      at least pa_decode_shared_prefix_workspace_size() bytes
  *                  (required: the two passes meet there). Its contents need
  *                  no initialisation; calls sharing it must not overlap.
- *   Other arguments as pa_decode. Supported: bf16 query and cache, head_dim
+ *   Other arguments as pa_decode. Supported: bf16 or fp16 query and cache, head_dim
  *   64 or 128, block_size 8, 16, 32, 64, 128 or 256. With no whole tile
  *   shared this is pa_decode.
  * ---------------------------------------------------------------------- */
@@ -249,7 +253,7 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
  * the time); [P1] "Why the attention kernel works at all" (the lookup cost
  * is amortised over a block, single-digit percent).
  *
- *   k, v         [num_seqs, max_seq_len, num_kv_heads, head_dim] bf16:
+ *   k, v         [num_seqs, max_seq_len, num_kv_heads, head_dim] bf16 or fp16:
  *                sequence b's token t at row b * max_seq_len + t. No block
  *                table: the same kernel as pa_decode, with the block id
  *                lookup replaced by the token offset.
@@ -259,7 +263,7 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
  *   max_context_len  host upper bound of context_lens, <= max_seq_len.
  *   workspace    as pa_decode, sized by pa_decode_workspace_size() with
  *                block_size 16.
- *   Other arguments as pa_decode. Supported: bf16 query and cache (F32
+ *   Other arguments as pa_decode. Supported: bf16 or fp16 query and cache (F32
  *   returns PA_ERR_UNSUPPORTED), head_dim 64 or 128,
  *   num_seqs * max_seq_len < 2^31.
  * ---------------------------------------------------------------------- */

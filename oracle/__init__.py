@@ -7,7 +7,8 @@ tables or helpers; neither imports the other). Only ``tests/``,
 
 Contents:
   * paged decode attention, whole-context and per-partition, and the
-    log-sum-exp merge (C, ``paged_attention.c``, via ctypes);
+    log-sum-exp merge (C, ``paged_attention.c``, via ctypes); caches and
+    queries are fp32, bf16 (as uint16 bits) or fp16, all widened exactly;
   * the slot scatter (reshape_and_cache), the block copy (copy_blocks) and the
     slot-id formula (numpy, ``cache_ops.py``);
   * a list-based model of the block manager (``block_manager_model.py``).
@@ -61,14 +62,17 @@ def _widen_query(query: np.ndarray, bf16: bool) -> np.ndarray:
 
 
 def _cache_args(k_cache: np.ndarray, v_cache: np.ndarray):
+    if v_cache.dtype != k_cache.dtype or v_cache.shape != k_cache.shape:
+        raise TypeError("k_cache and v_cache must match")
     if k_cache.dtype == np.uint16:
         bf16 = True
     elif k_cache.dtype == np.float32:
         bf16 = False
+    elif k_cache.dtype == np.float16:
+        # every fp16 value is an fp32 value: widening is exact
+        return k_cache.astype(np.float32), v_cache.astype(np.float32), False
     else:
-        raise TypeError("cache must be float32 or uint16 (bf16 bits)")
-    if v_cache.dtype != k_cache.dtype or v_cache.shape != k_cache.shape:
-        raise TypeError("k_cache and v_cache must match")
+        raise TypeError("cache must be float32, float16 or uint16 (bf16 bits)")
     return np.ascontiguousarray(k_cache), np.ascontiguousarray(v_cache), bf16
 
 

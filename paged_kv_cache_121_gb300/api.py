@@ -17,7 +17,7 @@ from . import _lib
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_BLOCKS = 0, 1, 2, 3
 PA_ERR_WORKSPACE, PA_ERR_TIMEOUT, PA_ERR_CUDA, PA_ERR_NOT_FOUND = 4, 5, 6, 7
-PA_F32, PA_BF16 = 0, 1
+PA_F32, PA_BF16, PA_F16 = 0, 1, 2
 
 
 class PAError(RuntimeError):
@@ -37,6 +37,8 @@ def _dtype(t: torch.Tensor) -> int:
         return PA_F32
     if t.dtype == torch.bfloat16:
         return PA_BF16
+    if t.dtype == torch.float16:
+        return PA_F16
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -112,7 +114,7 @@ def pa_decode_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_
 
 def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
               workspace=None, stream=None) -> None:
-    """Paged decode attention into ``out`` [B, Hq, D] (float32 or bfloat16).
+    """Paged decode attention into ``out`` [B, Hq, D] (float32, bfloat16 or float16).
 
     ``workspace`` is a zero-initialised uint8 tensor of at least
     :func:`pa_decode_workspace_size` bytes, or None (no context split)."""
@@ -162,7 +164,7 @@ def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_
 def pa_decode_contiguous(out, query, k, v, context_lens, max_context_len, scale, workspace=None,
                          stream=None) -> None:
     """Decode attention over a contiguous cache ``k``, ``v`` [B, max_seq_len,
-    Hkv, D] (bfloat16, no block table): the unpaged baseline. ``workspace``
+    Hkv, D] (bfloat16 or float16, no block table): the unpaged baseline. ``workspace``
     as for :func:`pa_decode`, sized with block_size 16."""
     B, L, hkv, d = (int(x) for x in k.shape)
     _, hq, _ = (int(x) for x in query.shape)

@@ -48,9 +48,12 @@ int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-int element_bytes(pa_dtype t) { return t == PA_BF16 ? 2 : 4; }
+int element_bytes(pa_dtype t) { return t == PA_F32 ? 4 : 2; }
 
-bool valid_dtype(pa_dtype t) { return t == PA_F32 || t == PA_BF16; }
+bool valid_dtype(pa_dtype t) { return t == PA_F32 || t == PA_BF16 || t == PA_F16; }
+
+// bf16 and fp16 share the tensor-core kernels (one instantiation each)
+bool is16(pa_dtype t) { return t == PA_BF16 || t == PA_F16; }
 
 pa_status current_device(int *dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return PA_ERR_CUDA;
@@ -166,7 +169,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // [head][half][token][128 bytes] (box_halves 0: every half). 128-byte
 // swizzle; out-of-range coordinates read as zeros.
 pa_status make_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int64_t block_size,
-                         int num_kv_heads, int head_dim, int box_tokens, int box_heads, int box_halves = 0) {
+                         int num_kv_heads, int head_dim, int box_tokens, int box_heads, int box_halves,
+                         bool f16) {
     auto enc = tensor_map_encoder();
     if (!enc) return PA_ERR_CUDA;
     const cuuint64_t halves = static_cast<cuuint64_t>(head_dim / 64);
@@ -178,7 +182,7 @@ pa_status make_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks
                                static_cast<cuuint32_t>(box_halves > 0 ? box_halves : static_cast<int>(halves)),
                                static_cast<cuuint32_t>(box_heads), 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims, strides,
+    CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
@@ -223,8 +227,8 @@ bool simt_forced() {
     return v;
 }
 
-bool use_mma(const DecodeShape &s, bool bf16) {
-    return bf16 && decode_mma_supported(s.head_dim, s.block_size) && !simt_forced();
+bool use_mma(const DecodeShape &s, bool kv16) {
+    return kv16 && decode_mma_supported(s.head_dim, s.block_size) && !simt_forced();
 }
 
 // Partition granularity: the tensor-core kernel's tile, the CUDA-core
@@ -359,7 +363,7 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
 // Decode of a wide split: partitions in split-K form into the workspace, then
 // the merge kernel on the same stream.
 pa_status launch_split_and_merge(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, bool mma,
-                                 int dev, void *workspace, const WorkspaceLayout &wl, void *out, bool out_bf16,
+                                 int dev, void *workspace, const WorkspaceLayout &wl, void *out, int out_type,
                                  cudaStream_t stream) {
     char *ws = static_cast<char *>(workspace);
     p.tmp_out = reinterpret_cast<float *>(ws + wl.o_off);
@@ -369,7 +373,7 @@ pa_status launch_split_and_merge(const DecodeShape &s, DecodeParams &p, pa_dtype
     p.cluster_merge = 0;
     pa_status st = launch_decode(s, p, kv_dtype, mma, dev, stream);
     if (st != PA_OK) return st;
-    const cudaError_t e = launch_lse_merge(out, out_bf16 ? 1 : 0, p.tmp_out, p.max_logits, p.exp_sums,
+    const cudaError_t e = launch_lse_merge(out, out_type, p.tmp_out, p.max_logits, p.exp_sums,
                                            p.context_lens, s.num_seqs, s.num_heads, s.head_dim,
                                            p.nsplit, p.part_tokens, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -385,7 +389,6 @@ pa_status check_dtypes(pa_dtype q_dtype, pa_dtype kv_dtype) {
 // kernel (bf16, a supported block size, partitions of whole 16-token tiles).
 pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype, bool mma, int dev,
                         cudaStream_t stream) {
-    const bool bf16 = kv_dtype == PA_BF16;
     p.status = status_word(dev);
     if (!p.status) return PA_ERR_CUDA;
     const dim3 grid(static_cast<unsigned>(p.nsplit),
@@ -406,13 +409,15 @@ pa_status launch_decode(const DecodeShape &s, DecodeParams &p, pa_dtype kv_dtype
         const int64_t map_blocks = contig ? 1 : s.num_blocks;
         const int64_t map_tokens = contig ? static_cast<int64_t>(s.num_seqs) * p.contig_stride : s.block_size;
         CUtensorMap tk, tv;
-        pa_status st = make_cache_map(&tk, p.k_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box, box_heads);
+        pa_status st = make_cache_map(&tk, p.k_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box, box_heads,
+                                      0, p.kv_f16 != 0);
         if (st != PA_OK) return st;
-        st = make_cache_map(&tv, p.v_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box, box_heads);
+        st = make_cache_map(&tv, p.v_cache, map_blocks, map_tokens, s.num_kv_heads, s.head_dim, box, box_heads, 0,
+                            p.kv_f16 != 0);
         if (st != PA_OK) return st;
         e = launch_decode_mma(p, tk, tv, grid, stream);
     } else {
-        e = launch_decode_simt(p, bf16, grid, stream);
+        e = launch_decode_simt(p, static_cast<int>(kv_dtype), grid, stream);
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -440,10 +445,10 @@ pa_status launch_balanced(const DecodeShape &s, DecodeParams &p, const Plan &pl,
     const int box = decode_mma_box_tokens(s.block_size);
     CUtensorMap tk, tv;
     pa_status st = make_cache_map(&tk, p.k_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim, box,
-                                  p.heads_per_cta);
+                                  p.heads_per_cta, 0, p.kv_f16 != 0);
     if (st != PA_OK) return st;
     if ((st = make_cache_map(&tv, p.v_cache, s.num_blocks, s.block_size, s.num_kv_heads, s.head_dim, box,
-                             p.heads_per_cta)) != PA_OK)
+                             p.heads_per_cta, 0, p.kv_f16 != 0)) != PA_OK)
         return st;
     const dim3 grid(static_cast<unsigned>(pl.bal_ctas),
                     static_cast<unsigned>((s.num_kv_heads / p.heads_per_cta) * p.ntile), 1u);
@@ -469,6 +474,7 @@ void fill_common(DecodeParams &p, const DecodeShape &s, const void *query, pa_dt
     p.num_blocks = s.num_blocks;
     p.group = s.num_heads / s.num_kv_heads;
     p.q_bf16 = q_dtype == PA_BF16;
+    p.kv_f16 = q_dtype == PA_F16;   // the caches have the query's type
     p.scale_log2 = scale * kLog2e;
 }
 
@@ -488,13 +494,14 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
     const int sms = sm_count(dev);
     if (sms <= 0) return PA_ERR_CUDA;
 
-    const Plan pl = plan_decode(s, sms, use_mma(s, kv_dtype == PA_BF16),
+    const Plan pl = plan_decode(s, sms, use_mma(s, is16(kv_dtype)),
                                 workspace != nullptr || workspace_bytes != 0, contig_stride == 0);
     DecodeParams p;
     fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
     p.contig_stride = contig_stride;
     p.out = out;
     p.out_bf16 = out_dtype == PA_BF16;
+    p.out_f16 = out_dtype == PA_F16;
     p.ntile = pl.ntile;
     p.heads_per_cta = pl.heads_per_cta;
     p.nsplit = pl.nsplit;
@@ -510,7 +517,7 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
     } else if (pl.nsplit > 1) {
         const WorkspaceLayout wl = workspace_layout(s, pl);
         if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-        return launch_split_and_merge(s, p, kv_dtype, pl.mma, dev, workspace, wl, out, out_dtype == PA_BF16,
+        return launch_split_and_merge(s, p, kv_dtype, pl.mma, dev, workspace, wl, out, static_cast<int>(out_dtype),
                                       as_stream(stream));
     } else {
         p.mode = kModeFinal;
@@ -586,7 +593,7 @@ pa_status check_prefix_call(const DecodeShape &s, pa_dtype q_dtype, pa_dtype kv_
     if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
     if (shared_blocks < 0 || shared_blocks > s.max_blocks) return PA_ERR_INVALID_ARG;
     // the prefix passes land one block (up to a tile) per TMA box: 8 rows or more
-    if (kv_dtype != PA_BF16 || !decode_mma_supported(s.head_dim, s.block_size) || s.block_size < 8)
+    if (!is16(kv_dtype) || !decode_mma_supported(s.head_dim, s.block_size) || s.block_size < 8)
         return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
@@ -608,7 +615,7 @@ int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes
     if ((st = current_device(&dev)) != PA_OK) return st;
     const int sms = sm_count(dev);
     if (sms <= 0) return PA_ERR_CUDA;
-    Plan pl = plan_split(s, sms, use_mma(s, kv_dtype == PA_BF16));
+    Plan pl = plan_split(s, sms, use_mma(s, is16(kv_dtype)));
     pl.cluster = false;   // the split, if any, goes through the scratch
     const WorkspaceLayout wl = workspace_layout(s, pl);
     if (pl.nsplit > 1 && (wl.total > scratch_bytes || !scratch || !aligned16(scratch)))
@@ -621,13 +628,14 @@ int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes
     fill_common(p, s, c.query, q_dtype, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale);
     p.out = c.out;
     p.out_bf16 = out_dtype == PA_BF16;
+    p.out_f16 = out_dtype == PA_F16;
     p.ntile = pl.ntile;
     p.heads_per_cta = pl.heads_per_cta;
     p.nsplit = pl.nsplit;
     p.part_tokens = pl.part_tokens;
     p.cluster_merge = 0;
     if (pl.nsplit > 1)
-        return launch_split_and_merge(s, p, kv_dtype, pl.mma, dev, scratch, wl, c.out, out_dtype == PA_BF16,
+        return launch_split_and_merge(s, p, kv_dtype, pl.mma, dev, scratch, wl, c.out, static_cast<int>(out_dtype),
                                       as_stream(stream));
     p.mode = kModeFinal;
     return launch_decode(s, p, kv_dtype, pl.mma, dev, as_stream(stream));
@@ -755,7 +763,7 @@ PA_API pa_status pa_decode_plan(int num_seqs, int num_heads, int num_kv_heads, i
     if ((st = current_device(&dev)) != PA_OK) return st;
     const int sms = sm_count(dev);
     if (sms <= 0) return PA_ERR_CUDA;
-    const Plan pl = plan_decode(s, sms, use_mma(s, kv_dtype == PA_BF16), with_workspace != 0);
+    const Plan pl = plan_decode(s, sms, use_mma(s, is16(kv_dtype)), with_workspace != 0);
     const bool wide = !pl.cluster && pl.nsplit > 1;
     plan->tensor_cores = pl.mma ? 1 : 0;
     plan->heads_per_cta = pl.heads_per_cta;
@@ -884,6 +892,7 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     pq.chunk_tokens = pp.chunk_tokens;
     pq.part_stride = pp.part_stride;
     pq.scale_log2 = scale * kLog2e;
+    pq.kv_f16 = kv_dtype == PA_F16;
     {
         const dim3 grid(static_cast<unsigned>(pp.chunks), static_cast<unsigned>(num_kv_heads),
                         static_cast<unsigned>(pp.row_groups));
@@ -893,8 +902,10 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
             const int box = std::min(block_size, prefix_tc_tile_tokens());
             const int stage = prefix_tc_stage_bytes(head_dim);
             pq.ring_bytes = std::max(stage, std::min(kTcMaxRingBytes, ring_kb() * 1024) / stage * stage);
-            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1)) != PA_OK ||
-                (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1)) != PA_OK) {
+            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1,
+                                     pq.kv_f16 != 0)) != PA_OK ||
+                (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1,
+                                     pq.kv_f16 != 0)) != PA_OK) {
                 join();
                 return st;
             }
@@ -906,8 +917,10 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
             const int box = decode_mma_box_tokens(block_size);
             const int stage = prefix_stage_bytes(head_dim);
             pq.ring_bytes = std::max(stage, std::min(kPrefixMaxRingBytes, ring_kb() * 1024) / stage * stage);
-            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK ||
-                (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1)) != PA_OK) {
+            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 0,
+                                     pq.kv_f16 != 0)) != PA_OK ||
+                (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 0,
+                                     pq.kv_f16 != 0)) != PA_OK) {
                 join();
                 return st;
             }
@@ -936,7 +949,7 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     if (!join() && st == PA_OK) st = PA_ERR_CUDA;
     if (st != PA_OK) return st;
     // 3. merge all partitions of every row
-    const cudaError_t e = launch_lse_merge(out, out_dtype == PA_BF16 ? 1 : 0, tmp_out, max_logits, exp_sums,
+    const cudaError_t e = launch_lse_merge(out, static_cast<int>(out_dtype), tmp_out, max_logits, exp_sums,
                                            context_lens, num_seqs, num_heads, head_dim, pp.part_stride, 0, strm);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -953,7 +966,7 @@ PA_API pa_status pa_decode_contiguous(void *out, pa_dtype out_dtype, const void 
     if (st != PA_OK) return st;
     if (!valid_dtype(out_dtype) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
     if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
-    if (kv_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (!is16(kv_dtype)) return PA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(num_seqs) * max_seq_len > INT32_MAX) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     return decode_planned(s, out, out_dtype, query, q_dtype, k, v, kv_dtype, nullptr, context_lens,
@@ -989,7 +1002,7 @@ PA_API pa_status pa_decode_splitk(float *tmp_out, float *max_logits, float *exp_
     p.max_logits = max_logits;
     p.exp_sums = exp_sums;
     // the tensor-core kernel cuts partitions at whole 16-token tiles
-    const bool mma = use_mma(s, kv_dtype == PA_BF16) &&
+    const bool mma = use_mma(s, is16(kv_dtype)) &&
                      partition_size % decode_mma_tile_tokens(block_size) == 0;
     p.ntile = (s.num_heads / s.num_kv_heads + kRowsPerTile - 1) / kRowsPerTile;
     p.heads_per_cta = mma ? decode_mma_heads_per_cta(s.num_kv_heads, heads_cap()) : 1;
@@ -1010,7 +1023,7 @@ PA_API pa_status pa_lse_merge(void *out, pa_dtype out_dtype, const float *tmp_ou
     if (num_seqs > 65535 || static_cast<size_t>(max_partitions) * sizeof(float) > 200 * 1024)
         return PA_ERR_UNSUPPORTED;
     if (!out || !tmp_out || !max_logits || !exp_sums || !context_lens) return PA_ERR_INVALID_ARG;
-    cudaError_t e = launch_lse_merge(out, out_dtype == PA_BF16, tmp_out, max_logits, exp_sums,
+    cudaError_t e = launch_lse_merge(out, static_cast<int>(out_dtype), tmp_out, max_logits, exp_sums,
                                      context_lens, num_seqs, num_heads, head_dim, max_partitions,
                                      partition_size, as_stream(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

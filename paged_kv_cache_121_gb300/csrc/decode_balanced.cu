@@ -1,5 +1,5 @@
 // Paged decode attention with the work of a ragged batch balanced across
-// CTAs, bf16 K/V, tensor cores, sm_103a.
+// CTAs, bf16 or fp16 K/V, tensor cores, sm_103a.
 //
 // What it computes: the same softmax(scale * q_h K^T) V per (sequence, query
 // head) as the per-partition kernel ("What Does PagedAttention Actually
@@ -98,10 +98,7 @@ __device__ __forceinline__ void prefetch_l1(const void *ptr) {
 }
 
 __device__ __forceinline__ void store_pair(const DecodeParams &p, int64_t idx, float a, float c) {
-    if (p.out_bf16)
-        *reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(p.out) + idx) = pack_bf16x2(a, c);
-    else
-        *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + idx) = make_float2(a, c);
+    store_pair_as(p.out, out_type_of(p), idx, a, c);
 }
 
 // A finished segment of sequence b for query heads h0 .. h0+rows-1: the
@@ -143,7 +140,7 @@ __device__ __forceinline__ void segment_epilogue(const DecodeParams &p, const Wa
     }
 }
 
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(32 * (kMaxHeads + 1), 1)
 decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        const __grid_constant__ DecodeParams p, const __grid_constant__ BalancedParams bp) {
@@ -278,7 +275,7 @@ decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
                 while (P[b + 1] <= g) ++b;   // skip empty sequences
                 len = attended_len(p, bp, b);
                 seg_end = P[b + 1];
-                const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.query);
+                const uint16_t *qb = static_cast<const uint16_t *>(p.query);
                 const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
                     qb + (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D);
                 load_query_fragments<D>(qa, q0, q0 + 8 * (D / 2), r < rows, r + 8 < rows, lane);
@@ -289,7 +286,7 @@ decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
                 int nb = b + 1;
                 while (nb < B && P[nb + 1] == P[nb]) ++nb;
                 if (nb < B && P[nb] < end) {
-                    const __nv_bfloat16 *n0 = qb + (static_cast<int64_t>(nb) * p.num_heads + h0 + r) * D;
+                    const uint16_t *n0 = qb + (static_cast<int64_t>(nb) * p.num_heads + h0 + r) * D;
 #pragma unroll
                     for (int x = 0; x < D * 2; x += 128) {
                         if (r < rows) prefetch_l1(reinterpret_cast<const char *>(n0) + x);
@@ -316,7 +313,8 @@ decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
                 }
                 __syncwarp();
             }
-            warp_tile_attention<D, kTT>(st, qa, kbase, kbase + v_off, kHalfStride, tok_off, valid, valid, sl2, lane);
+            warp_tile_attention<D, kTT, true, kF16>(st, qa, kbase, kbase + v_off, kHalfStride, tok_off, valid, valid,
+                                                    sl2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[kMaxStages + s]));
         }
@@ -410,10 +408,10 @@ __global__ void __launch_bounds__(128) balanced_merge_kernel(const __grid_consta
     for (int e = 0; e < E; e += 2) store_pair(p, o + e, acc[e], acc[e + 1]);
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t launch_balanced_dim(const DecodeParams &p, const BalancedParams &bp, const CUtensorMap &tk,
                                 const CUtensorMap &tv, dim3 grid, cudaStream_t stream) {
-    auto kern = decode_balanced_kernel<D>;
+    auto kern = decode_balanced_kernel<D, kF16>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, smem_bytes(kMaxRingBytes, kBalancedMaxSeqs), done);
     if (e != cudaSuccess) return e;
@@ -435,8 +433,12 @@ cudaError_t launch_decode_balanced(const DecodeParams &p, const BalancedParams &
     if (p.num_seqs < 1 || p.num_seqs > kBalancedMaxSeqs || p.ring_bytes > kMaxRingBytes || bp.ctas < 1 ||
         p.heads_per_cta < 1 || p.heads_per_cta > kMaxHeads)
         return cudaErrorInvalidValue;
-    if (p.head_dim == 128) return launch_balanced_dim<128>(p, bp, tk, tv, grid, stream);
-    if (p.head_dim == 64) return launch_balanced_dim<64>(p, bp, tk, tv, grid, stream);
+    if (p.head_dim == 128)
+        return p.kv_f16 ? launch_balanced_dim<128, true>(p, bp, tk, tv, grid, stream)
+                        : launch_balanced_dim<128, false>(p, bp, tk, tv, grid, stream);
+    if (p.head_dim == 64)
+        return p.kv_f16 ? launch_balanced_dim<64, true>(p, bp, tk, tv, grid, stream)
+                        : launch_balanced_dim<64, false>(p, bp, tk, tv, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -1,4 +1,4 @@
-// Paged decode attention, bf16 K/V, tensor-core kernel for sm_103a.
+// Paged decode attention, bf16 or fp16 K/V, tensor-core kernel for sm_103a.
 //
 // What it computes: for each sequence b and query head h, softmax(scale *
 // q_h K^T) V over the sequence's tokens, with K and V fetched block by block
@@ -24,7 +24,7 @@
 //    every stage. S = Q K^T runs on the tensor cores (mma.m16n8k16, M = the
 //    query heads of the GQA group, N = tokens, K = head dims; Q stays in
 //    registers). Online softmax in base 2 with a running max and sum per row.
-//    P is split into a bf16 high part and a bf16 residual so that P.V (M =
+//    P is split into a 16-bit high part and a residual so that P.V (M =
 //    heads, N = head dims, K = tokens) keeps ~16 bits of P. Each warp
 //    releases the stage with one mbarrier arrive; the stage is refilled once
 //    every head's warp has released it.
@@ -62,10 +62,7 @@ struct MmaCfg {
 };
 
 __device__ __forceinline__ void store_out2(const DecodeParams &p, int64_t idx, float a, float c) {
-    if (p.out_bf16)
-        *reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(p.out) + idx) = pack_bf16x2(a, c);
-    else
-        *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + idx) = make_float2(a, c);
+    store_pair_as(p.out, out_type_of(p), idx, a, c);
 }
 
 
@@ -200,7 +197,7 @@ __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, co
 enum LoadMode { kLoadBox = 0, kLoadPairs = 1, kLoadRows = 2 };
 static_assert(MmaCfg<128, 16>::producers(kLoadRows) == 2 && MmaCfg<128, 16>::producers(kLoadBox) == 1, "");
 
-template <int D, int TT, bool kCluster, int kLoad>
+template <int D, int TT, bool kCluster, int kLoad, bool kF16>
 __global__ void __launch_bounds__(32 * (MmaCfg<D, TT>::kMaxHeads + MmaCfg<D, TT>::producers(kLoad)), 1)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
@@ -416,7 +413,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         uint32_t qa[D / 16][4];
         {
             const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
-                static_cast<const __nv_bfloat16 *>(p.query) +
+                static_cast<const uint16_t *>(p.query) +
                 (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D);
             load_query_fragments<D>(qa, q0, q0 + 8 * (D / 2), r < rows, r + 8 < rows, lane);
         }
@@ -445,7 +442,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 __syncwarp();
             }
 
-            warp_tile_attention<D, TT, !kRows>(st, qa, kbase, vbase, kHalfStride, tok_off, valid, valid, sl2, lane);
+            warp_tile_attention<D, TT, !kRows, kF16>(st, qa, kbase, vbase, kHalfStride, tok_off, valid, valid, sl2,
+                                                     lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[C::kMaxStages + s]));
         }
@@ -470,20 +468,20 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
-template <int D, int TT, int kLoad>
+template <int D, int TT, int kLoad, bool kF16>
 static cudaError_t launch_impl(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                dim3 grid, cudaStream_t stream) {
     using C = MmaCfg<D, TT>;
     const size_t smem = C::smem_bytes(p.ring_bytes);
     const dim3 block(32 * (p.heads_per_cta + C::producers(kLoad)));
     if (!p.cluster_merge) {
-        auto kern = decode_mma_kernel<D, TT, false, kLoad>;
+        auto kern = decode_mma_kernel<D, TT, false, kLoad, kF16>;
         static unsigned long long done = 0;
         cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
         if (e != cudaSuccess) return e;
         return launch_kernel(kern, grid, block, smem, stream, 1u, tk, tv, p);
     }
-    auto kern = decode_mma_kernel<D, TT, true, kLoad>;
+    auto kern = decode_mma_kernel<D, TT, true, kLoad, kF16>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(C::kMaxRingBytes), done);
     if (e != cudaSuccess) return e;
@@ -530,20 +528,24 @@ int decode_mma_load_mode(int block_size, bool contiguous) {
     return block_size == 8 ? kLoadPairs : kLoadRows;   // blocks of 8: two per 16-token tile
 }
 
-template <int D>
+template <int D, bool kF16>
 static cudaError_t launch_for_dim(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                   dim3 grid, cudaStream_t stream) {
     switch (decode_mma_load_mode(p.block_size, p.contig_stride > 0)) {
-        case kLoadBox: return launch_impl<D, 16, kLoadBox>(p, tk, tv, grid, stream);
-        case kLoadPairs: return launch_impl<D, 16, kLoadPairs>(p, tk, tv, grid, stream);
-        default: return launch_impl<D, 16, kLoadRows>(p, tk, tv, grid, stream);
+        case kLoadBox: return launch_impl<D, 16, kLoadBox, kF16>(p, tk, tv, grid, stream);
+        case kLoadPairs: return launch_impl<D, 16, kLoadPairs, kF16>(p, tk, tv, grid, stream);
+        default: return launch_impl<D, 16, kLoadRows, kF16>(p, tk, tv, grid, stream);
     }
 }
 
 cudaError_t launch_decode_mma(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                               dim3 grid, cudaStream_t stream) {
-    if (p.head_dim == 128) return launch_for_dim<128>(p, tk, tv, grid, stream);
-    if (p.head_dim == 64) return launch_for_dim<64>(p, tk, tv, grid, stream);
+    if (p.head_dim == 128)
+        return p.kv_f16 ? launch_for_dim<128, true>(p, tk, tv, grid, stream)
+                        : launch_for_dim<128, false>(p, tk, tv, grid, stream);
+    if (p.head_dim == 64)
+        return p.kv_f16 ? launch_for_dim<64, true>(p, tk, tv, grid, stream)
+                        : launch_for_dim<64, false>(p, tk, tv, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -1,5 +1,5 @@
-// Paged decode attention on the CUDA cores (fp32 caches, and bf16 caches
-// whose block size the tensor-core kernel does not take), plus the
+// Paged decode attention on the CUDA cores (fp32 caches, and bf16 or fp16
+// caches whose block size the tensor-core kernel does not take), plus the
 // log-sum-exp merge of split-K partitions.
 //
 // Same work decomposition and epilogue as the tensor-core kernel: one CTA per
@@ -52,6 +52,24 @@ struct RowLoad<E, __nv_bfloat16> {
     }
 };
 
+template <int E>
+struct RowLoad<E, __half> {
+    __device__ static void load(const __half *row, float (&x)[E]) {
+        if constexpr (E == 4) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(row);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+            const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+            x[0] = a.x; x[1] = a.y; x[2] = c.x; x[3] = c.y;
+        } else if constexpr (E == 2) {
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(row));
+            x[0] = a.x; x[1] = a.y;
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[e] = __half2float(row[e]);
+        }
+    }
+};
+
 template <int D, int MAXR, typename KV>
 __global__ void __launch_bounds__(128)
 decode_simt_kernel(const __grid_constant__ DecodeParams p) {
@@ -82,10 +100,7 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
         for (int e = 0; e < E; ++e) o[r][e] = q[r][e] = 0.f;
         if (r < rows) {
             const int64_t off = (static_cast<int64_t>(b) * p.num_heads + h0 + r) * D + lane * E;
-            if (p.q_bf16)
-                RowLoad<E, __nv_bfloat16>::load(static_cast<const __nv_bfloat16 *>(p.query) + off, q[r]);
-            else
-                RowLoad<E, float>::load(static_cast<const float *>(p.query) + off, q[r]);
+            RowLoad<E, KV>::load(static_cast<const KV *>(p.query) + off, q[r]);   // the query has the caches' type
         }
     }
 
@@ -165,13 +180,16 @@ static cudaError_t launch_simt_rows(const DecodeParams &p, dim3 grid, cudaStream
     return launch_simt_impl<D, 16, KV>(p, grid, stream);
 }
 
-cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, cudaStream_t stream) {
-    if (p.head_dim == 128)
-        return kv_bf16 ? launch_simt_rows<128, __nv_bfloat16>(p, grid, stream)
-                       : launch_simt_rows<128, float>(p, grid, stream);
-    if (p.head_dim == 64)
-        return kv_bf16 ? launch_simt_rows<64, __nv_bfloat16>(p, grid, stream)
-                       : launch_simt_rows<64, float>(p, grid, stream);
+template <int D>
+static cudaError_t launch_simt_dim(const DecodeParams &p, int kv_type, dim3 grid, cudaStream_t stream) {
+    if (kv_type == 1) return launch_simt_rows<D, __nv_bfloat16>(p, grid, stream);
+    if (kv_type == 2) return launch_simt_rows<D, __half>(p, grid, stream);
+    return launch_simt_rows<D, float>(p, grid, stream);
+}
+
+cudaError_t launch_decode_simt(const DecodeParams &p, int kv_type, dim3 grid, cudaStream_t stream) {
+    if (p.head_dim == 128) return launch_simt_dim<128>(p, kv_type, grid, stream);
+    if (p.head_dim == 64) return launch_simt_dim<64>(p, kv_type, grid, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -179,7 +197,7 @@ cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, c
 // log-sum-exp merge of split-K partitions: one CTA per (head, sequence)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128)
-lse_merge_kernel(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
+lse_merge_kernel(void *out, int out_type, const float *tmp_out, const float *max_logits,
                  const float *exp_sums, const int32_t *context_lens, int num_heads, int head_dim,
                  int max_partitions, int partition_size) {
     extern __shared__ float wgt[];  // [max_partitions]
@@ -220,14 +238,16 @@ lse_merge_kernel(void *out, int out_bf16, const float *tmp_out, const float *max
 #pragma unroll 8
         for (int q = 0; q < np; ++q) acc += wgt[q] * __ldcg(src + static_cast<int64_t>(q) * head_dim);
         const int64_t oi = (static_cast<int64_t>(b) * num_heads + h) * head_dim + d;
-        if (out_bf16)
+        if (out_type == 1)
             reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(acc * inv);
+        else if (out_type == 2)
+            reinterpret_cast<__half *>(out)[oi] = __float2half_rn(acc * inv);
         else
             reinterpret_cast<float *>(out)[oi] = acc * inv;
     }
 }
 
-cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
+cudaError_t launch_lse_merge(void *out, int out_type, const float *tmp_out, const float *max_logits,
                              const float *exp_sums, const int32_t *context_lens, int num_seqs,
                              int num_heads, int head_dim, int max_partitions, int partition_size,
                              cudaStream_t stream) {
@@ -238,7 +258,7 @@ cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, cons
         if (e != cudaSuccess) return e;
     }
     dim3 grid(num_heads, num_seqs);
-    return launch_kernel(lse_merge_kernel, grid, dim3(128), smem, stream, 1u, out, out_bf16, tmp_out,
+    return launch_kernel(lse_merge_kernel, grid, dim3(128), smem, stream, 1u, out, out_type, tmp_out,
                          max_logits, exp_sums, context_lens, num_heads, head_dim, max_partitions,
                          partition_size);
 }

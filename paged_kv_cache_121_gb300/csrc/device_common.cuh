@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <cstdlib>
@@ -50,8 +51,10 @@ struct DecodeParams {
     int part_stride;     // split-K rows: partitions per (sequence, head) in tmp_out (0: nsplit)
     int part_offset;     //   and the index of this launch's partition 0 there
     int mode;
-    int out_bf16;
+    int out_bf16;        // output element: bf16, else fp16 if out_f16, else fp32
+    int out_f16;
     int q_bf16;
+    int kv_f16;          // 16-bit query and caches are fp16 (else bf16)
     float scale_log2;    // scale * log2(e): scores are kept in base-2 units
 };
 
@@ -119,6 +122,7 @@ struct PrefixParams {
     int chunk_tokens;             // tokens per chunk (a multiple of 16)
     int part_stride;              // partitions per row in tmp_out
     int ring_bytes;
+    int kv_f16;                   // query and caches are fp16 (else bf16)
     float scale_log2;
 };
 
@@ -156,10 +160,29 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
+
+// Two fp32 values into the output element type (out_type: 0 fp32, 1 bf16,
+// 2 fp16, as the public dtype codes), at out + idx (idx even).
+__device__ __forceinline__ void store_pair_as(void *out, int out_type, int64_t idx, float a, float c) {
+    if (out_type == 1)
+        *reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(out) + idx) = pack_bf16x2(a, c);
+    else if (out_type == 2)
+        *reinterpret_cast<uint32_t *>(static_cast<__half *>(out) + idx) = pack_f16x2(a, c);
+    else
+        *reinterpret_cast<float2 *>(static_cast<float *>(out) + idx) = make_float2(a, c);
+}
+
+// The decode's output element type as a dtype code.
+__device__ __forceinline__ int out_type_of(const DecodeParams &p) { return p.out_bf16 ? 1 : p.out_f16 ? 2 : 0; }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -335,6 +358,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The m16n8k16 product for 16-bit inputs of either kind.
+template <bool kF16>
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (kF16) mma_f16_16816(c, a, b0, b1);
+    else mma_bf16_16816(c, a, b0, b1);
+}
+
 // Split-K row of (sequence b, query head h, partition part) in tmp_out /
 // max_logits / exp_sums.
 __device__ __forceinline__ int64_t split_row(const DecodeParams &p, int b, int h, int part) {
@@ -420,6 +459,8 @@ __device__ void combine_warps(float *base, int nwarps, int rows) {
 __device__ __forceinline__ void store_out(const DecodeParams &p, int64_t idx, float v) {
     if (p.out_bf16)
         reinterpret_cast<__nv_bfloat16 *>(p.out)[idx] = __float2bfloat16_rn(v);
+    else if (p.out_f16)
+        reinterpret_cast<__half *>(p.out)[idx] = __float2half_rn(v);
     else
         reinterpret_cast<float *>(p.out)[idx] = v;
 }

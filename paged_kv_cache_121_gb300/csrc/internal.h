@@ -48,8 +48,9 @@ size_t decode_balanced_smem_extra(int num_seqs);
 cudaError_t launch_decode_balanced(const DecodeParams &p, const BalancedParams &bp, const CUtensorMap &tmap_k,
                                    const CUtensorMap &tmap_v, dim3 grid, cudaStream_t stream);
 cudaError_t launch_balanced_merge(const DecodeParams &p, const BalancedParams &bp, cudaStream_t stream);
-cudaError_t launch_decode_simt(const DecodeParams &p, bool kv_bf16, dim3 grid, cudaStream_t stream);
-cudaError_t launch_lse_merge(void *out, int out_bf16, const float *tmp_out, const float *max_logits,
+// kv_type / out_type: 0 fp32, 1 bf16, 2 fp16 (the public dtype codes)
+cudaError_t launch_decode_simt(const DecodeParams &p, int kv_type, dim3 grid, cudaStream_t stream);
+cudaError_t launch_lse_merge(void *out, int out_type, const float *tmp_out, const float *max_logits,
                              const float *exp_sums, const int32_t *context_lens, int num_seqs,
                              int num_heads, int head_dim, int max_partitions, int partition_size,
                              cudaStream_t stream);

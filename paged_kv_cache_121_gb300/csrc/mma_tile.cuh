@@ -2,7 +2,8 @@
 // (one m16 tile) against one 16-token tile of K and V in shared memory,
 // with a base-2 online softmax ("What Does PagedAttention Actually
 // Optimize?", section 8: softmax(scale q K^T) V, computed block by block).
-// Shared by the paged decode kernel and the shared-prefix kernel.
+// Shared by the paged decode kernels and the shared-prefix kernel; bf16 or
+// fp16 inputs (kF16), fp32 accumulation.
 //
 // Shared-memory tile layout: for each 64-dim half of the head dimension, 16
 // token rows of 128 bytes; row t of half c lives at base + c * half_stride +
@@ -22,6 +23,21 @@ __device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t &hi, uin
     const float hx = bf16_bits_to_float(hi & 0xffffu);
     const float hy = bf16_bits_to_float(hi >> 16);
     lo = pack_bf16x2(x - hx, y - hy);
+}
+
+__device__ __forceinline__ void split_f16x2(float x, float y, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    const float2 hf = __half22float2(h);
+    lo = pack_f16x2(x - hf.x, y - hf.y);
+}
+
+// P (probabilities in [0, 1]) as a 16-bit high part plus a 16-bit residual,
+// in the element type of the products.
+template <bool kF16>
+__device__ __forceinline__ void split_x2(float x, float y, uint32_t &hi, uint32_t &lo) {
+    if constexpr (kF16) split_f16x2(x, y, hi, lo);
+    else split_bf16x2(x, y, hi, lo);
 }
 
 // One warp's softmax state for 16 query rows of one KV head, in the mma
@@ -49,7 +65,7 @@ struct WarpState {
     }
 };
 
-// The A fragments of the warp's 16 query rows (bf16, D dims): q0 / q1 point at
+// The A fragments of the warp's 16 query rows (16-bit, D dims): q0 / q1 point at
 // rows r and r + 8 (lane r = lane / 4); a row that is not live reads as zeros.
 template <int D>
 __device__ __forceinline__ void load_query_fragments(uint32_t (&qa)[D / 16][4], const uint32_t *q0,
@@ -68,7 +84,7 @@ __device__ __forceinline__ void load_query_fragments(uint32_t (&qa)[D / 16][4], 
 // S = Q K^T for the tile, masking, online softmax update, O += P V. Tokens at
 // or past valid0 (row r) / valid1 (row r + 8) get score -inf. V rows of tokens
 // past the tile's data must already hold zeros (0 * NaN would leak).
-template <int D, int TT, bool kSwizzled = true, typename TokOff>
+template <int D, int TT, bool kSwizzled = true, bool kF16 = false, typename TokOff>
 __device__ __forceinline__ void warp_tile_attention(WarpState<D> &st, const uint32_t (&qa)[D / 16][4],
                                                     uint32_t kbase, uint32_t vbase, int half_stride,
                                                     TokOff tok_off, int valid0, int valid1, float sl2,
@@ -91,8 +107,8 @@ __device__ __forceinline__ void warp_tile_attention(WarpState<D> &st, const uint
                                   (((c & 7) ^ (kSwizzled ? tok & 7 : 0)) << 4);
             uint32_t b0, b1, b2, b3;
             ldmatrix_x4(addr, b0, b1, b2, b3);
-            mma_bf16_16816(sacc[j], qa[kk], b0, b1);
-            mma_bf16_16816(acc2, qa[kk + 1], b2, b3);
+            mma_16816<kF16>(sacc[j], qa[kk], b0, b1);
+            mma_16816<kF16>(acc2, qa[kk + 1], b2, b3);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[j][e] = (sacc[j][e] + acc2[e]) * sl2;
@@ -149,11 +165,11 @@ __device__ __forceinline__ void warp_tile_attention(WarpState<D> &st, const uint
         const float p2 = fast_exp2(sacc[j][2] - mn1), p3 = fast_exp2(sacc[j][3] - mn1);
         st.l0 += p0 + p1;
         st.l1 += p2 + p3;
-        split_bf16x2(p0, p1, phi[2 * j], plo[2 * j]);
-        split_bf16x2(p2, p3, phi[2 * j + 1], plo[2 * j + 1]);
+        split_x2<kF16>(p0, p1, phi[2 * j], plo[2 * j]);
+        split_x2<kF16>(p2, p3, phi[2 * j + 1], plo[2 * j + 1]);
     }
 
-    // ---- O += P V (P as a bf16 high part plus a bf16 residual) ----
+    // ---- O += P V (P as a 16-bit high part plus a 16-bit residual) ----
 #pragma unroll
     for (int dn = 0; dn < D / 8; dn += 2) {
         const int mi = lane >> 3;
@@ -163,10 +179,10 @@ __device__ __forceinline__ void warp_tile_attention(WarpState<D> &st, const uint
                               (((c & 7) ^ (kSwizzled ? tok & 7 : 0)) << 4);
         uint32_t v0, v1, v2, v3;
         ldmatrix_x4_trans(addr, v0, v1, v2, v3);
-        mma_bf16_16816(st.o[dn], phi, v0, v1);
-        mma_bf16_16816(st.o[dn + 1], phi, v2, v3);
-        mma_bf16_16816(st.o[dn], plo, v0, v1);
-        mma_bf16_16816(st.o[dn + 1], plo, v2, v3);
+        mma_16816<kF16>(st.o[dn], phi, v0, v1);
+        mma_16816<kF16>(st.o[dn + 1], phi, v2, v3);
+        mma_16816<kF16>(st.o[dn], plo, v0, v1);
+        mma_16816<kF16>(st.o[dn + 1], plo, v2, v3);
     }
 }
 

@@ -1,4 +1,4 @@
-// Shared-prefix attention pass, bf16 K/V, tensor cores, sm_103a.
+// Shared-prefix attention pass, bf16 or fp16 K/V, tensor cores, sm_103a.
 //
 // What it computes. When every sequence of a batch starts with the same
 // physical blocks (a prompt prefix shared by reference count: "PagedAttention:
@@ -42,7 +42,7 @@ struct PrefixCfg {
     static size_t smem_bytes(int ring) { return 1024 + static_cast<size_t>(ring) + kBarrierBytes; }
 };
 
-template <int D, bool kPairs>
+template <int D, bool kPairs, bool kF16>
 __global__ void __launch_bounds__(kPrefixThreads, 2)
 prefix_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ PrefixParams p) {
@@ -155,7 +155,7 @@ prefix_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         len1 = min(max(len1, 0), p.prefix_tokens);
         uint32_t qa[D / 16][4];
         {
-            const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.query);
+            const uint16_t *q = static_cast<const uint16_t *>(p.query);
             const uint32_t *q0 = reinterpret_cast<const uint32_t *>(
                 q + (static_cast<int64_t>(b0) * p.num_heads + hq0) * D);
             const uint32_t *q1 = reinterpret_cast<const uint32_t *>(
@@ -180,7 +180,7 @@ prefix_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             const uint32_t kbase = smem_addr(smem + s * stage_bytes);
             const int t0 = tok_begin + i * TT;
             const int valid0 = min(TT, max(0, len0 - t0)), valid1 = min(TT, max(0, len1 - t0));
-            warp_tile_attention<D, TT>(st, qa, kbase, kbase + v_off, kHalfStride, tok_off, valid0, valid1,
+            warp_tile_attention<D, TT, true, kF16>(st, qa, kbase, kbase + v_off, kHalfStride, tok_off, valid0, valid1,
                                        sl2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars[kPrefixMaxStages + s]));
@@ -223,11 +223,11 @@ prefix_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
 }
 
-template <int D, bool kPairs>
+template <int D, bool kPairs, bool kF16>
 cudaError_t launch_prefix_impl(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
                                cudaStream_t stream) {
     using C = PrefixCfg<D>;
-    auto kern = prefix_mma_kernel<D, kPairs>;
+    auto kern = prefix_mma_kernel<D, kPairs, kF16>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(kPrefixMaxRingBytes), done);
     if (e != cudaSuccess) return e;
@@ -243,12 +243,20 @@ int prefix_stage_bytes(int head_dim) { return 2 * kPrefixTile * head_dim * 2; }
 cudaError_t launch_prefix_mma(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
                               cudaStream_t stream) {
     const bool pairs = p.block_size < kPrefixTile;
-    if (p.head_dim == 128)
-        return pairs ? launch_prefix_impl<128, true>(p, tk, tv, grid, stream)
-                     : launch_prefix_impl<128, false>(p, tk, tv, grid, stream);
-    if (p.head_dim == 64)
-        return pairs ? launch_prefix_impl<64, true>(p, tk, tv, grid, stream)
-                     : launch_prefix_impl<64, false>(p, tk, tv, grid, stream);
+    if (p.head_dim == 128) {
+        if (p.kv_f16)
+            return pairs ? launch_prefix_impl<128, true, true>(p, tk, tv, grid, stream)
+                         : launch_prefix_impl<128, false, true>(p, tk, tv, grid, stream);
+        return pairs ? launch_prefix_impl<128, true, false>(p, tk, tv, grid, stream)
+                     : launch_prefix_impl<128, false, false>(p, tk, tv, grid, stream);
+    }
+    if (p.head_dim == 64) {
+        if (p.kv_f16)
+            return pairs ? launch_prefix_impl<64, true, true>(p, tk, tv, grid, stream)
+                         : launch_prefix_impl<64, false, true>(p, tk, tv, grid, stream);
+        return pairs ? launch_prefix_impl<64, true, false>(p, tk, tv, grid, stream)
+                     : launch_prefix_impl<64, false, false>(p, tk, tv, grid, stream);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -21,7 +21,7 @@
 //    their row of S from tensor memory, run the base-2 online softmax in
 //    registers (a row per thread: no shuffles), rescale their row of O in
 //    tensor memory when the running max moves by more than 8 (rare), and
-//    write P as a bf16 high part and a bf16 residual into one of two shared
+//    write P as a 16-bit high part and a residual into one of two shared
 //    buffers (tile i + 1's softmax does not wait for tile i's P.V).
 //  * Warp 4 streams the tiles' K and V with TMA (one box per block, 64-dim
 //    half and cache) into a ring of stages guarded by mbarriers; it fills
@@ -35,6 +35,7 @@
 // its own MMAs and copies (bounded), frees its tensor memory and returns.
 #include "device_common.cuh"
 #include "internal.h"
+#include "mma_tile.cuh"
 #include "tcgen05.cuh"
 
 namespace pa {
@@ -82,7 +83,7 @@ __device__ __forceinline__ bool tc_wait(const PrefixParams &p, TcBars *bars, uin
     return false;
 }
 
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                  const __grid_constant__ PrefixParams p) {
@@ -168,7 +169,7 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const bool live = R < nrows;
         const int b = live ? R / p.group : 0;
         const int hq = g * p.group + (live ? R % p.group : 0);
-        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.query) +
+        const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.query) +
                                                            (static_cast<int64_t>(b) * p.num_heads + hq) * D);
 #pragma unroll
         for (int h = 0; h < C::kHalves; ++h)
@@ -201,8 +202,8 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     } else if (warp == 5) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            constexpr uint32_t id_qk = idesc_bf16_f32(kTcRows, kTcTile, false, false);
-            constexpr uint32_t id_pv = idesc_bf16_f32(kTcRows, D, false, true);
+            constexpr uint32_t id_qk = idesc_16bit_f32(kTcRows, kTcTile, false, false, kF16);
+            constexpr uint32_t id_pv = idesc_16bit_f32(kTcRows, D, false, true, kF16);
             const uint32_t q_base = smem_addr(q_s);
             auto issue_pv = [&](int i) -> bool {   // O += P V for tile i (P buffer i % 2)
                 const int pb = i & 1;
@@ -213,9 +214,9 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
                 for (int kk = 0; kk < kTcTile / 16; ++kk) {
                     const uint64_t bdesc = smem_desc_sw128(vbase + kk * 16 * 128, kTcTile * 128, 1024);
-                    tc_mma_bf16(tmem + C::kOCol, smem_desc_sw128(hi + kk * 32, 16, 1024), bdesc, id_pv,
+                    tc_mma_16bit(tmem + C::kOCol, smem_desc_sw128(hi + kk * 32, 16, 1024), bdesc, id_pv,
                                 (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_mma_bf16(tmem + C::kOCol, smem_desc_sw128(lo + kk * 32, 16, 1024), bdesc, id_pv, 1u);
+                    tc_mma_16bit(tmem + C::kOCol, smem_desc_sw128(lo + kk * 32, 16, 1024), bdesc, id_pv, 1u);
                 }
                 tc_commit(smem_addr(&bars->pv_done[pb]));
                 tc_commit(smem_addr(&bars->empty[i % nstages]));
@@ -231,7 +232,7 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t half = kk / 4, off = (kk % 4) * 32;
-                    tc_mma_bf16(tmem + C::kSCol0 + b * kTcTile,
+                    tc_mma_16bit(tmem + C::kSCol0 + b * kTcTile,
                                 smem_desc_sw128(q_base + half * (kTcRows * 128) + off, 16, 1024),
                                 smem_desc_sw128(kbase + half * (kTcTile * 128) + off, 16, 1024), id_qk,
                                 kk > 0 ? 1u : 0u);
@@ -307,9 +308,7 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 for (int e = 0; e < 4; ++e) {
                     const float p0 = fast_exp2(s[8 * c + 2 * e] - m), p1 = fast_exp2(s[8 * c + 2 * e + 1] - m);
                     l += p0 + p1;
-                    hi[e] = pack_bf16x2(p0, p1);
-                    lo[e] = pack_bf16x2(p0 - bf16_bits_to_float(hi[e] & 0xffffu),
-                                        p1 - bf16_bits_to_float(hi[e] >> 16));
+                    split_x2<kF16>(p0, p1, hi[e], lo[e]);   // P in the type of V
                 }
                 const int pos = row * 128 + ((c ^ (row & 7)) << 4);
                 *reinterpret_cast<uint4 *>(hi_b + pos) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -363,11 +362,11 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
 }
 
-template <int D>
+template <int D, bool kF16>
 cudaError_t launch_tc_impl(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
                            cudaStream_t stream) {
     using C = TcCfg<D>;
-    auto kern = prefix_tc_kernel<D>;
+    auto kern = prefix_tc_kernel<D, kF16>;
     static unsigned long long done = 0;
     cudaError_t e = ensure_smem_limit(kern, C::smem_bytes(kTcMaxRingBytes), done);
     if (e != cudaSuccess) return e;
@@ -382,8 +381,12 @@ int prefix_tc_stage_bytes(int head_dim) { return 2 * (head_dim / 64) * kTcTile *
 
 cudaError_t launch_prefix_tc(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv, dim3 grid,
                              cudaStream_t stream) {
-    if (p.head_dim == 128) return launch_tc_impl<128>(p, tk, tv, grid, stream);
-    if (p.head_dim == 64) return launch_tc_impl<64>(p, tk, tv, grid, stream);
+    if (p.head_dim == 128)
+        return p.kv_f16 ? launch_tc_impl<128, true>(p, tk, tv, grid, stream)
+                        : launch_tc_impl<128, false>(p, tk, tv, grid, stream);
+    if (p.head_dim == 64)
+        return p.kv_f16 ? launch_tc_impl<64, true>(p, tk, tv, grid, stream)
+                        : launch_tc_impl<64, false>(p, tk, tv, grid, stream);
     return cudaErrorInvalidValue;
 }
 

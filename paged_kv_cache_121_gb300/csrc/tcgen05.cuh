@@ -28,19 +28,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulate.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor for kind::f16 with fp32 accumulate: A and B both
+// bf16, or both fp16 (f16_inputs); the two never differ.
+__host__ __device__ constexpr uint32_t idesc_16bit_f32(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                       bool f16_inputs) {
     return (1u << 4)                                      // D: f32
-           | (1u << 7)                                    // A: bf16
-           | (1u << 10)                                   // B: bf16
+           | (f16_inputs ? 0u : (1u << 7))                // A: fp16 (0) or bf16 (1)
+           | (f16_inputs ? 0u : (1u << 10))               // B: the same type as A
            | (a_mn_major ? (1u << 15) : 0u)
            | (b_mn_major ? (1u << 16) : 0u)
            | (static_cast<uint32_t>(N >> 3) << 17)
            | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]; one thread issues.
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+// D[tmem] (+)= A[smem] * B[smem] for 16-bit inputs (their type is in the
+// instruction descriptor); one thread issues.
+__device__ __forceinline__ void tc_mma_16bit(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"

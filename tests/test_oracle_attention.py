@@ -274,3 +274,47 @@ def test_pins_catch_planted_mistake(tmp_path, name):
         except (AssertionError, ValueError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutation {name}"
+
+
+def test_oracle_fp16_inputs():
+    """fp16 caches and queries are widened exactly ("What Does PagedAttention
+    Actually Optimize?", section 2: fp16 and bf16 both two bytes a value).
+    Pinned two ways: a one-token context returns its V row, bit for bit, at
+    the edges of the fp16 range; and a random fp16 batch through the paged
+    pool equals torch SDPA on the dense, widened arrays."""
+    edge = np.array([65504.0, -65504.0, 2.0 ** -14, 2.0 ** -24, -0.0, 1.0 / 3.0, -2.5, 1.0], np.float16)
+    hkv, d, bs = 1, 64, 16
+    v = np.zeros((4, bs, hkv, d), np.float16)
+    k = np.zeros_like(v)
+    v[2, 0, 0, :8] = edge
+    v[2, 0, 0, 8:] = np.float16(0.75)
+    k[2, 0, 0, :] = np.float16(0.5)
+    q = np.full((1, 2, d), np.float16(-1.25), np.float16)
+    out = oracle.paged_attention(q, k, v, np.array([[2]], np.int32), np.array([1], np.int32), 0.125)
+    for h in range(2):
+        assert np.array_equal(out[0, h], v[2, 0, 0].astype(np.float64))
+
+    rng = np.random.default_rng(31)
+    lens = [37, 5, 64]
+    hq, hkv, d, bs = 8, 2, 64, 16
+    dk = [rng.standard_normal((n, hkv, d)).astype(np.float16) for n in lens]
+    dv = [rng.standard_normal((n, hkv, d)).astype(np.float16) for n in lens]
+    q = rng.standard_normal((len(lens), hq, d)).astype(np.float16)
+    kpool = np.zeros((12, bs, hkv, d), np.float16)
+    vpool = np.zeros_like(kpool)
+    tables = np.zeros((len(lens), 4), np.int32)
+    perm = rng.permutation(12)
+    pos = 0
+    for b, n in enumerate(lens):
+        nb = -(-n // bs)
+        for j in range(nb):
+            rows = slice(j * bs, min(n, (j + 1) * bs))
+            kpool[perm[pos], :rows.stop - rows.start] = dk[b][rows]
+            vpool[perm[pos], :rows.stop - rows.start] = dv[b][rows]
+            tables[b, j] = perm[pos]
+            pos += 1
+    out = oracle.paged_attention(q, kpool, vpool, tables, np.array(lens, np.int32), d ** -0.5)
+    for b, n in enumerate(lens):
+        want = sdpa_reference(q[b].astype(np.float64), dk[b].astype(np.float64), dv[b].astype(np.float64),
+                              d ** -0.5)
+        assert np.max(np.abs(out[b] - want)) < 1e-12

@@ -8,7 +8,8 @@ the kernels and in the oracle).
 
 Recipe (fixed seeds, numpy PCG64 ``default_rng``):
   * seed 121: K/V/query values, N(0, 1) drawn in fp32, then rounded to bf16
-    with round-to-nearest-even (the toy case stays fp32);
+    (or, for fp16 batches, to fp16) with round-to-nearest-even (the toy case
+    stays fp32);
   * seed 122: physical block placement, ``rng.permutation(num_blocks)`` taken
     in order, one id per logical block, sequence after sequence;
   * seed 123: context lengths and shared-prefix suffix lengths.
@@ -52,9 +53,11 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _normal(rng: np.random.Generator, shape, bf16: bool) -> np.ndarray:
+def _normal(rng: np.random.Generator, shape, bf16: bool, f16: bool = False) -> np.ndarray:
     x = rng.standard_normal(shape, dtype=np.float32)
-    return bf16_round(x) if bf16 else x
+    if bf16:
+        return bf16_round(x)
+    return x.astype(np.float16) if f16 else x
 
 
 def cdiv(a: int, b: int) -> int:
@@ -69,8 +72,8 @@ class DecodeBatch:
     """One decode step's inputs.
 
     Arrays (row-major, numpy):
-      query        [B, Hq, D]                 float32, or uint16 bf16 bits
-      k_cache      [num_blocks, BS, Hkv, D]   float32, or uint16 bf16 bits
+      query        [B, Hq, D]                 float32, float16, or uint16 bf16 bits
+      k_cache      [num_blocks, BS, Hkv, D]   float32, float16, or uint16 bf16 bits
       v_cache      same as k_cache
       block_tables [B, max_blocks] int32, entries past a sequence's blocks = 0
       context_lens [B] int32 (the number of tokens attended, new token included)
@@ -93,6 +96,7 @@ class DecodeBatch:
     head_dim: int
     scale: float
     bf16: bool
+    f16: bool = False
 
     @property
     def num_seqs(self) -> int:
@@ -112,7 +116,7 @@ class DecodeBatch:
 
     @property
     def elem_bytes(self) -> int:
-        return 2 if self.bf16 else 4
+        return 2 if self.bf16 or self.f16 else 4
 
 
 def place_blocks(context_lens: np.ndarray, block_size: int, num_blocks: int,
@@ -140,43 +144,46 @@ def place_blocks(context_lens: np.ndarray, block_size: int, num_blocks: int,
 def make_batch(name: str, context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
                block_size: int, num_blocks: int, bf16: bool, max_blocks: Optional[int] = None,
                seed_values: int = SEED_VALUES, seed_blocks: int = SEED_BLOCKS,
-               fill_unused: bool = False) -> DecodeBatch:
+               fill_unused: bool = False, f16: bool = False) -> DecodeBatch:
     """Draw a decode batch.
 
     Every slot of every block a sequence owns gets an N(0,1) draw, the tail
     slots of its last block included (so a kernel that forgets to mask them
     gives a wrong answer). Blocks nobody owns stay zero unless ``fill_unused``.
+    ``f16`` (with ``bf16`` False): the draws are rounded to fp16 instead.
     """
     lens = np.asarray(context_lens, dtype=np.int32)
     B = lens.size
     tables = place_blocks(lens, block_size, num_blocks, max_blocks, seed_blocks)
     rng = np.random.default_rng(seed_values)
-    dt = np.uint16 if bf16 else np.float32
+    f16 = f16 and not bf16
+    dt = np.uint16 if bf16 else np.float16 if f16 else np.float32
     shape = (num_blocks, block_size, num_kv_heads, head_dim)
     k_cache = np.zeros(shape, dtype=dt)
     v_cache = np.zeros(shape, dtype=dt)
     used = [tables[i, :cdiv(int(n), block_size)] for i, n in enumerate(lens)]
     used = np.concatenate(used) if used else np.zeros(0, np.int32)
     if fill_unused:
-        k_cache[...] = _normal(rng, shape, bf16)
-        v_cache[...] = _normal(rng, shape, bf16)
+        k_cache[...] = _normal(rng, shape, bf16, f16)
+        v_cache[...] = _normal(rng, shape, bf16, f16)
     elif used.size:
-        k_cache[used] = _normal(rng, (used.size,) + shape[1:], bf16)
-        v_cache[used] = _normal(rng, (used.size,) + shape[1:], bf16)
-    query = _normal(rng, (B, num_heads, head_dim), bf16)
-    new_key = _normal(rng, (B, num_kv_heads, head_dim), bf16)
-    new_value = _normal(rng, (B, num_kv_heads, head_dim), bf16)
+        k_cache[used] = _normal(rng, (used.size,) + shape[1:], bf16, f16)
+        v_cache[used] = _normal(rng, (used.size,) + shape[1:], bf16, f16)
+    query = _normal(rng, (B, num_heads, head_dim), bf16, f16)
+    new_key = _normal(rng, (B, num_kv_heads, head_dim), bf16, f16)
+    new_value = _normal(rng, (B, num_kv_heads, head_dim), bf16, f16)
     return DecodeBatch(name=name, query=query, k_cache=k_cache, v_cache=v_cache,
                        block_tables=tables, context_lens=lens, new_key=new_key,
                        new_value=new_value, new_pos=np.maximum(lens - 1, 0).astype(np.int32),
                        block_size=block_size, num_heads=num_heads, num_kv_heads=num_kv_heads,
-                       head_dim=head_dim, scale=1.0 / math.sqrt(head_dim), bf16=bf16)
+                       head_dim=head_dim, scale=1.0 / math.sqrt(head_dim), bf16=bf16, f16=f16)
 
 
 def shared_prefix_batch(name: str, shared_blocks: int, suffix_lens, num_heads: int, num_kv_heads: int,
                         head_dim: int, block_size: int, spare_blocks: int = 7,
-                        seed_values: int = SEED_VALUES, seed_blocks: int = SEED_BLOCKS) -> DecodeBatch:
-    """A bf16 decode batch whose sequences share their first ``shared_blocks``
+                        seed_values: int = SEED_VALUES, seed_blocks: int = SEED_BLOCKS,
+                        f16: bool = False) -> DecodeBatch:
+    """A bf16 (``f16``: fp16) decode batch whose sequences share their first ``shared_blocks``
     (full) blocks: every table row starts with the same physical ids, then
     each sequence's private blocks for ``suffix_lens[b]`` more tokens. Ids
     are a seeded permutation of a pool with ``spare_blocks`` unused blocks."""
@@ -195,19 +202,19 @@ def shared_prefix_batch(name: str, shared_blocks: int, suffix_lens, num_heads: i
         pos += n
     rng = np.random.default_rng(seed_values)
     shape = (num_blocks, block_size, num_kv_heads, head_dim)
-    k_cache = np.zeros(shape, dtype=np.uint16)
-    v_cache = np.zeros(shape, dtype=np.uint16)
+    k_cache = np.zeros(shape, dtype=np.float16 if f16 else np.uint16)
+    v_cache = np.zeros_like(k_cache)
     used = perm[:pos]
-    k_cache[used] = _normal(rng, (used.size,) + shape[1:], True)
-    v_cache[used] = _normal(rng, (used.size,) + shape[1:], True)
-    query = _normal(rng, (B, num_heads, head_dim), True)
-    new_key = _normal(rng, (B, num_kv_heads, head_dim), True)
-    new_value = _normal(rng, (B, num_kv_heads, head_dim), True)
+    k_cache[used] = _normal(rng, (used.size,) + shape[1:], not f16, f16)
+    v_cache[used] = _normal(rng, (used.size,) + shape[1:], not f16, f16)
+    query = _normal(rng, (B, num_heads, head_dim), not f16, f16)
+    new_key = _normal(rng, (B, num_kv_heads, head_dim), not f16, f16)
+    new_value = _normal(rng, (B, num_kv_heads, head_dim), not f16, f16)
     return DecodeBatch(name=name, query=query, k_cache=k_cache, v_cache=v_cache, block_tables=tables,
                        context_lens=lens, new_key=new_key, new_value=new_value,
                        new_pos=np.maximum(lens - 1, 0).astype(np.int32), block_size=block_size,
                        num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
-                       scale=1.0 / math.sqrt(head_dim), bf16=True)
+                       scale=1.0 / math.sqrt(head_dim), bf16=not f16, f16=f16)
 
 
 # --------------------------------------------------------------------------
@@ -275,8 +282,8 @@ class ContiguousBatch:
     sequence owns ``max_seq_len`` consecutive rows, as under a per-request
     maximum-length reservation.
 
-      query        [B, Hq, D]              uint16 bf16 bits
-      k, v         [B, max_seq_len, Hkv, D] uint16 bf16 bits; rows at or past a
+      query        [B, Hq, D]              uint16 bf16 bits (float16 when not bf16)
+      k, v         [B, max_seq_len, Hkv, D] uint16 bf16 bits (or float16); rows at or past a
                    sequence's length hold zeros, or NaN with ``tail_nan``
       context_lens [B] int32
       new_key, new_value [B, Hkv, D]; new_pos [B] (= context_len - 1)
@@ -316,29 +323,33 @@ BF16_NAN_BITS = 0x7FC0
 
 
 def contiguous(name: str, context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
-               max_seq_len: int, tail_nan: bool = False, seed_values: int = SEED_VALUES) -> ContiguousBatch:
-    """Draw a bf16 decode batch in the contiguous layout (N(0,1) rows for each
-    sequence's tokens, seeded like ``make_batch``)."""
+               max_seq_len: int, tail_nan: bool = False, seed_values: int = SEED_VALUES,
+               f16: bool = False) -> ContiguousBatch:
+    """Draw a bf16 (``f16``: fp16) decode batch in the contiguous layout
+    (N(0,1) rows for each sequence's tokens, seeded like ``make_batch``)."""
     lens = np.asarray(context_lens, dtype=np.int32)
     B = lens.size
     if B and int(lens.max()) > max_seq_len:
         raise ValueError("a length exceeds max_seq_len")
     rng = np.random.default_rng(seed_values)
     shape = (B, max_seq_len, num_kv_heads, head_dim)
-    fill = np.uint16(BF16_NAN_BITS) if tail_nan else np.uint16(0)
-    k = np.full(shape, fill, dtype=np.uint16)
-    v = np.full(shape, fill, dtype=np.uint16)
+    if f16:
+        dt, fill = np.float16, (np.float16(np.nan) if tail_nan else np.float16(0))
+    else:
+        dt, fill = np.uint16, (np.uint16(BF16_NAN_BITS) if tail_nan else np.uint16(0))
+    k = np.full(shape, fill, dtype=dt)
+    v = np.full(shape, fill, dtype=dt)
     for b in range(B):
         n = int(lens[b])
-        k[b, :n] = _normal(rng, (n, num_kv_heads, head_dim), True)
-        v[b, :n] = _normal(rng, (n, num_kv_heads, head_dim), True)
-    query = _normal(rng, (B, num_heads, head_dim), True)
-    new_key = _normal(rng, (B, num_kv_heads, head_dim), True)
-    new_value = _normal(rng, (B, num_kv_heads, head_dim), True)
+        k[b, :n] = _normal(rng, (n, num_kv_heads, head_dim), not f16, f16)
+        v[b, :n] = _normal(rng, (n, num_kv_heads, head_dim), not f16, f16)
+    query = _normal(rng, (B, num_heads, head_dim), not f16, f16)
+    new_key = _normal(rng, (B, num_kv_heads, head_dim), not f16, f16)
+    new_value = _normal(rng, (B, num_kv_heads, head_dim), not f16, f16)
     return ContiguousBatch(name=name, query=query, k=k, v=v, context_lens=lens, new_key=new_key,
                            new_value=new_value, new_pos=np.maximum(lens - 1, 0).astype(np.int32),
                            num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
-                           scale=1.0 / math.sqrt(head_dim))
+                           scale=1.0 / math.sqrt(head_dim), bf16=not f16)
 
 
 @dataclasses.dataclass

@@ -4,16 +4,18 @@
 One step = one pass of the hot path over one batch: the new token of every
 sequence is scattered into its slot (pa_reshape_and_cache), then paged
 decode attention runs over the whole context (pa_decode, context split across
-CTAs and merged by log-sum-exp in the last CTA). The default workload is the
+CTAs and merged by log-sum-exp). The default workload is the
 Qwen3-8B-shaped layer: 16 sequences x 4,164 tokens, 32 query / 8 KV heads,
 head_dim 128, bf16, blocks of 16 scattered over a 38,348-block pool.
 
 Prints ONE JSON line (rank 0). ``value`` is KV GB/s: the bytes of K and V a
 decode step must read (valid tokens only) divided by the device time per step,
 with inputs resident in HBM. Two batches alternate so that consecutive steps
-read disjoint 273 MB sets (L2 is 129 MB). ``e2e`` repeats the measurement
-through the public API with the step's inputs copied from pinned host memory
-and the output read back every step.
+read disjoint 273 MB sets (L2 is 129 MB). ``e2e`` is the wall-clock rate of
+the same steps with every step's inputs copied from pinned host memory and
+its output copied back and read on the host; copies run on their own stream
+beside the kernels (captured from the public calls into CUDA graphs), a few
+steps in flight.
 
 ``--impl reference`` times the oracle (fp64 CPU) on the host cores instead,
 one bounded sample of the workload per step.
@@ -40,6 +42,7 @@ import workloads  # noqa: E402
 
 HBM_NOMINAL_GBS = 8000.0
 GRAPH_STEPS = 20          # steps captured per CUDA graph in the timed loop
+E2E_DEPTH = 3             # e2e steps in flight before the host reads a step's output
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -360,13 +363,13 @@ def run_ours(args, rank, world, local_rank):
     def scatter(v):
         pa.pa_reshape_and_cache(v["key"], v["value"], k_cache, v_cache, v["slots"])
 
-    def decode_into(out, v, query, lens, tables):
+    def decode_into(out, v, query, lens, tables, stream=None):
         if contig:
             pa.pa_decode_contiguous(out, query, v["k"], v["v"], lens, v["max_len"], batch.scale,
-                                    workspace=workspace)
+                                    workspace=workspace, stream=stream)
         else:
             pa.pa_decode(out, query, k_cache, v_cache, tables, lens, v["max_len"], batch.scale,
-                         workspace=workspace)
+                         workspace=workspace, stream=stream)
 
     def decode(v):
         decode_into(v["out"], v, v["query"], v["lens"], v["tables"])
@@ -462,59 +465,122 @@ def run_ours(args, rank, world, local_rank):
     decode_ms = e0.elapsed_time(e1) / (dreps * GRAPH_STEPS)
     scatter_ms, _ = time_graph(torch, stream, lambda i: scatter(views[i % copies]), dreps)
 
-    # e2e through the public API, host buffers (pinned), copies inside the timed region
-    h_in = []
-    for c in range(copies):
-        sl = slice(c * nb, (c + 1) * nb)
-        h_in.append({
-            "query": torch.from_numpy(batch.query[sl].view(np.int16).copy()).pin_memory(),
-            "tables": None if contig else torch.from_numpy(batch.block_tables[sl].copy()).pin_memory(),
-            "lens": torch.from_numpy(batch.context_lens[sl].copy()).pin_memory(),
-            "key": torch.from_numpy(batch.new_key[sl].view(np.int16).copy()).pin_memory(),
-            "value": torch.from_numpy(batch.new_value[sl].view(np.int16).copy()).pin_memory(),
-            "slots": torch.from_numpy(slots_all[sl].copy()).pin_memory(),
-            "out": torch.empty((nb, hq, d), dtype=torch.float32).pin_memory(),
-        })
-    h2d = sum(h_in[0][k].numel() * h_in[0][k].element_size()
-              for k in ("query", "tables", "lens", "key", "value", "slots") if h_in[0][k] is not None)
-    d2h = h_in[0]["out"].numel() * 4
-    dq = torch.empty((nb, hq, d), dtype=torch.bfloat16, device="cuda")
-    dk = torch.empty((nb, hkv, d), dtype=torch.bfloat16, device="cuda")
-    dvv = torch.empty_like(dk)
-    dt = None if contig else torch.empty_like(views[0]["tables"])
-    dl = torch.empty_like(views[0]["lens"])
-    ds = torch.empty_like(views[0]["slots"])
-    dout = torch.empty((nb, hq, d), dtype=torch.float32, device="cuda")
+    # e2e through the public API, host buffers (pinned), copies inside the timed
+    # region. Every step copies its inputs (query, new K/V, tables, lengths,
+    # slots: one packed pinned buffer, one transfer) to the device, runs the
+    # scatter and the decode (captured once from the public calls into a CUDA
+    # graph per buffer set, as a serving engine captures its decode step),
+    # and copies the output back to pinned host memory, where the host reads
+    # it. Steps are pipelined E2E_DEPTH deep over two streams ordered by
+    # events: the kernels on one, the copies on the other, where step i + 1's
+    # upload is queued before step i's download, so that both overlap the
+    # kernels. The host reads a step's output when it comes back to that
+    # step's buffers.
+    def pack(arrays):
+        offs, pos = [], 0
+        for a in arrays:
+            offs.append(pos)
+            pos += (a.nbytes + 255) // 256 * 256
+        buf = np.zeros(pos, np.uint8)
+        for a, o in zip(arrays, offs):
+            buf[o:o + a.nbytes] = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+        return torch.from_numpy(buf).pin_memory(), offs
 
-    def e2e_step(i):
-        h = h_in[i % copies]
-        v = views[i % copies]
-        dq.view(torch.int16).copy_(h["query"], non_blocking=True)
-        dk.view(torch.int16).copy_(h["key"], non_blocking=True)
-        dvv.view(torch.int16).copy_(h["value"], non_blocking=True)
-        if dt is not None:
-            dt.copy_(h["tables"], non_blocking=True)
-        dl.copy_(h["lens"], non_blocking=True)
-        ds.copy_(h["slots"], non_blocking=True)
-        pa.pa_reshape_and_cache(dk, dvv, k_cache, v_cache, ds)
-        decode_into(dout, v, dq, dl, dt)
-        h["out"].copy_(dout, non_blocking=True)
-        torch.cuda.current_stream().synchronize()   # the result is read on the host
-        return float(h["out"][0, 0, 0])
+    def host_arrays(c):
+        sl = slice(c * nb, (c + 1) * nb)
+        arrs = [batch.query[sl], batch.new_key[sl], batch.new_value[sl], batch.context_lens[sl],
+                slots_all[sl].astype(np.int64)]
+        if not contig:
+            arrs.append(batch.block_tables[sl])
+        return arrs
+
+    staged = [pack(host_arrays(c)) for c in range(copies)]
+    h2d = staged[0][0].numel()
+    kv_t = k_cache.dtype
+    arr0 = host_arrays(0)
+    offs0 = staged[0][1]
+    s_e2e, s_copy = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def slot_buffers():
+        stage = torch.empty(h2d, dtype=torch.uint8, device="cuda")
+
+        def view(i, dtype, shape):
+            o = offs0[i]
+            n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+            return stage[o:o + n].view(dtype).view(shape)
+
+        sb = {"stage": stage, "q": view(0, kv_t, arr0[0].shape), "k": view(1, kv_t, arr0[1].shape),
+              "v": view(2, kv_t, arr0[2].shape), "lens": view(3, torch.int32, arr0[3].shape),
+              "slots": view(4, torch.int64, arr0[4].shape),
+              "tables": None if contig else view(5, torch.int32, arr0[5].shape),
+              "out": torch.empty((nb, hq, d), dtype=torch.float32, device="cuda"),
+              "h_out": torch.empty((nb, hq, d), dtype=torch.float32).pin_memory(),
+              "up": torch.cuda.Event(), "run": torch.cuda.Event(), "down": torch.cuda.Event(),
+              "pending": False, "graphs": []}
+        for c in range(copies):
+            with torch.cuda.stream(s_e2e):
+                sb["stage"].copy_(staged[c][0])
+                for _ in range(2):   # warm up outside the capture
+                    pa.pa_reshape_and_cache(sb["k"], sb["v"], k_cache, v_cache, sb["slots"])
+                    decode_into(sb["out"], views[c], sb["q"], sb["lens"], sb["tables"])
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s_e2e, capture_error_mode="thread_local"):
+                pa.pa_reshape_and_cache(sb["k"], sb["v"], k_cache, v_cache, sb["slots"])
+                decode_into(sb["out"], views[c], sb["q"], sb["lens"], sb["tables"])
+            sb["graphs"].append(g)
+        return sb
+
+    slots_e2e = [slot_buffers() for _ in range(E2E_DEPTH)]
+    d2h = slots_e2e[0]["h_out"].numel() * 4
+    checksum = [0.0]
+
+    def read_back(sb):
+        if sb["pending"]:
+            sb["down"].synchronize()
+            checksum[0] += float(sb["h_out"][0, 0, 0])   # the step's result, read on the host
+            sb["pending"] = False
+
+    def upload(i):   # on s_copy
+        sb = slots_e2e[i % E2E_DEPTH]
+        read_back(sb)   # the buffers' previous step is done: they are free
+        sb["stage"].copy_(staged[i % copies][0], non_blocking=True)
+        sb["up"].record(s_copy)
+
+    def e2e_step(i):   # current stream: s_e2e
+        sb = slots_e2e[i % E2E_DEPTH]
+        s_e2e.wait_event(sb["up"])
+        sb["graphs"][i % copies].replay()
+        sb["run"].record(s_e2e)
+        with torch.cuda.stream(s_copy):
+            upload(i + 1)   # the next step's inputs go up while this step runs
+            s_copy.wait_event(sb["run"])
+            sb["h_out"].copy_(sb["out"], non_blocking=True)
+            sb["down"].record(s_copy)
+        sb["pending"] = True
+
+    def e2e_run(n):
+        with torch.cuda.stream(s_copy):
+            upload(0)
+        with torch.cuda.stream(s_e2e):
+            for i in range(n):
+                e2e_step(i)
+        for sb in slots_e2e:
+            read_back(sb)
 
     e2e_steps = min(K, 2000)
-    for i in range(3):
-        e2e_step(i)
+    e2e_run(E2E_DEPTH + 1)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
+    e2e_run(e2e_steps)
     e2e_s = time.perf_counter() - t0
     torch.cuda.synchronize()
     if pa.pa_device_status() != 0:
         raise SystemExit("device status not clean after the timed region")
+    if not np.isfinite(checksum[0]):
+        raise SystemExit("non-finite decode output in the e2e loop")
 
     # max over ranks
     ms_step = ms_total / steps_timed

@@ -85,6 +85,9 @@ def load() -> ctypes.CDLL:
     Raises if the library cannot be built or loaded: there is no other
     implementation to fall back to."""
     global _lib
+    lib = _lib
+    if lib is not None:   # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is None:
             path = _build.build()

@@ -47,13 +47,13 @@ def _ptr(t: Optional[torch.Tensor]):
         return None
     if not t.is_contiguous():
         raise ValueError("tensors passed to libpa must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()   # an int: ctypes converts it through the c_void_p argtype
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _cache_dims(k_cache: torch.Tensor) -> Tuple[int, int, int, int]:

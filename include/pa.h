@@ -206,6 +206,24 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
                            size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * One decode step: pa_reshape_and_cache of the step's new tokens, then
+ * pa_decode ([P3] steps 4 and 5: write the new key and value into their
+ * slots, then attend over the whole context through the block table).
+ * The same two launches, in order, as the two calls; the arguments of both
+ * are checked before either is launched, so a refused call writes nothing.
+ *   key, value, slot_mapping, num_tokens   as pa_reshape_and_cache
+ *   every other argument                   as pa_decode
+ * ---------------------------------------------------------------------- */
+PA_API pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
+                                  const void *key, const void *value, const int64_t *slot_mapping,
+                                  int num_tokens, void *k_cache, void *v_cache, pa_dtype kv_dtype,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_blocks_per_seq, int num_blocks,
+                                  int max_context_len, float scale, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Decode attention for a batch whose sequences share their leading blocks.
  * [P1] "Copy-on-write: when two requests share a prefix" (several block
  * tables point at the same physical blocks, reference-counted); [P5]

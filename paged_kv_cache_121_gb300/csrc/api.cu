@@ -682,6 +682,32 @@ PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, void *
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+PA_API pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
+                                  const void *key, const void *value, const int64_t *slot_mapping,
+                                  int num_tokens, void *k_cache, void *v_cache, pa_dtype kv_dtype,
+                                  const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                                  int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_context_len, float scale,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    // every check of both calls first, so that a refused call launches nothing
+    const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        max_blocks_per_seq, num_blocks, max_context_len};
+    pa_status st = check_shape(s);
+    if (st != PA_OK) return st;
+    if (!valid_dtype(out_dtype) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
+    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value)))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && !block_tables) return PA_ERR_INVALID_ARG;
+    if ((st = pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
+                                   block_size, num_kv_heads, head_dim, kv_dtype, stream)) != PA_OK)
+        return st;
+    if (num_seqs == 0) return PA_OK;
+    return decode_planned(s, out, out_dtype, query, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                          context_lens, 0, scale, workspace, workspace_bytes, stream);
+}
+
 PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
                                 int num_pairs, int num_blocks, int block_size, int num_kv_heads,
                                 int head_dim, pa_dtype kv_dtype, void *stream) {

@@ -1,0 +1,117 @@
+"""pa_decode_append: the step's scatter and decode in one call ("PagedAttention,
+explained.", procedure steps 4 and 5). The result must be the oracle's
+(scatter, then attention over the updated cache) and bit-for-bit the result
+of the two calls made separately, on every decode path: cluster and
+per-partition, each load mode, the wide split with its merge kernel, the
+ragged-balanced path, fp16; a refused call writes nothing."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_121_gb300 as pa
+import workloads
+from gpu_cases import (ATOL, DeviceBatch, make_workspace, max_err, new_token_slots, oracle_step,
+                       to_host_bits)
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # lens, Hq, Hkv, D, block size, f16, workspace
+    ((1, 2, 15, 16, 17, 100, 333), 8, 2, 128, 16, False, False),   # cluster merge
+    ((3000, 4000), 16, 4, 128, 16, False, True),                   # wide split + merge kernel
+    ((1, 7, 8, 9, 64, 250), 16, 4, 128, 8, False, True),           # two blocks per tile
+    ((19, 90, 300), 8, 2, 128, 4, True, True),                     # bulk row copies, fp16
+    ((40, 90), 8, 2, 64, 12, False, True),                         # CUDA-core kernel
+]
+
+
+def run_append(db, ws, out_dtype=torch.float32):
+    b = db.h
+    slots = torch.from_numpy(new_token_slots(b)).cuda()
+    out = torch.empty((b.num_seqs, b.num_heads, b.head_dim), dtype=out_dtype, device="cuda")
+    pa.pa_decode_append(out, db.query, db.new_key, db.new_value, slots, db.k_cache, db.v_cache, db.block_tables,
+                        db.context_lens, b.max_context_len, b.scale, workspace=ws)
+    return out
+
+
+def run_separate(db, ws, out_dtype=torch.float32):
+    b = db.h
+    slots = torch.from_numpy(new_token_slots(b)).cuda()
+    pa.pa_reshape_and_cache(db.new_key, db.new_value, db.k_cache, db.v_cache, slots)
+    out = torch.empty((b.num_seqs, b.num_heads, b.head_dim), dtype=out_dtype, device="cuda")
+    pa.pa_decode(out, db.query, db.k_cache, db.v_cache, db.block_tables, db.context_lens, b.max_context_len,
+                 b.scale, workspace=ws)
+    return out
+
+
+def bits(t):
+    return t.cpu().view(torch.int16).numpy() if t.element_size() == 2 else to_host_bits(t)
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_append_matches_oracle_and_separate_calls(case):
+    lens, hq, hkv, d, bs, f16, use_ws = CASES[case]
+    need = sum(workloads.cdiv(n, bs) for n in lens)
+    batch = workloads.make_batch("append", lens, hq, hkv, d, bs, need + 9, not f16, seed_values=900 + case,
+                                 f16=f16)
+    db = DeviceBatch(batch)
+    ws = make_workspace(batch) if use_ws else None
+    out = run_append(db, ws)
+    want, k_want, v_want = oracle_step(batch)
+    assert np.array_equal(bits(db.k_cache), np.ascontiguousarray(k_want).view(np.int16))
+    assert np.array_equal(bits(db.v_cache), np.ascontiguousarray(v_want).view(np.int16))
+    assert max_err(out, want) <= ATOL
+    # the same two calls made separately, on a fresh copy of the inputs
+    db2 = DeviceBatch(batch)
+    out2 = run_separate(db2, make_workspace(batch) if use_ws else None)
+    assert torch.equal(out, out2)
+    torch.cuda.synchronize()
+    assert pa.pa_device_status(clear=True) == 0
+
+
+def test_append_balanced_and_in_a_graph():
+    rng = np.random.default_rng(950)
+    lens = rng.integers(1, 600, size=160).astype(np.int32)
+    need = sum(workloads.cdiv(int(n), 16) for n in lens)
+    batch = workloads.make_batch("append_bal", lens, 32, 8, 128, 16, need + 9, True, seed_values=951)
+    assert pa.pa_decode_plan(160, 32, 8, 128, 16, int(lens.max()), with_workspace=True)["balanced"]
+    db = DeviceBatch(batch)
+    ws = make_workspace(batch)
+    slots = torch.from_numpy(new_token_slots(batch)).cuda()
+    out = torch.empty((160, 32, 128), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        pa.pa_decode_append(out, db.query, db.new_key, db.new_value, slots, db.k_cache, db.v_cache,
+                            db.block_tables, db.context_lens, batch.max_context_len, batch.scale, workspace=ws)
+    torch.cuda.synchronize()
+    want, _, _ = oracle_step(batch)
+    assert max_err(out, want) <= ATOL
+    # captured and replayed: the scatter rewrites the same values, the decode gives the same output
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        pa.pa_decode_append(out, db.query, db.new_key, db.new_value, slots, db.k_cache, db.v_cache,
+                            db.block_tables, db.context_lens, batch.max_context_len, batch.scale, workspace=ws)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert max_err(out, want) <= ATOL
+    assert pa.pa_device_status(clear=True) == 0
+
+
+def test_append_refuses_before_launching():
+    """A shape the decode refuses (8 query heads over 3 KV heads) launches
+    nothing: the scatter must not have written its rows either."""
+    batch = workloads.make_batch("append_bad", (10, 20), 8, 2, 128, 16, 8, True, seed_values=960)
+    db = DeviceBatch(batch)
+    before = bits(db.k_cache).copy()
+    slots = torch.from_numpy(new_token_slots(batch)).cuda()
+    out = torch.empty((2, 8, 128), dtype=torch.float32, device="cuda")
+    status = pa.load_library().pa_decode_append(
+        out.data_ptr(), pa.PA_F32, db.query.data_ptr(), pa.PA_BF16, db.new_key.data_ptr(), db.new_value.data_ptr(),
+        slots.data_ptr(), 2, db.k_cache.data_ptr(), db.v_cache.data_ptr(), pa.PA_BF16, db.block_tables.data_ptr(),
+        db.context_lens.data_ptr(), 2, 8, 3, 128, 16, int(db.block_tables.shape[1]), 8, 20, 0.1, None, 0,
+        torch.cuda.current_stream().cuda_stream)
+    assert status == pa.PA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(db.k_cache), before)

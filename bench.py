@@ -2,9 +2,10 @@
 """Benchmark of the paged-KV decode hot path on GB300.
 
 One step = one pass of the hot path over one batch: the new token of every
-sequence is scattered into its slot (pa_reshape_and_cache), then paged
-decode attention runs over the whole context (pa_decode, context split across
-CTAs and merged by log-sum-exp). The default workload is the
+sequence is written into its slot, then paged decode attention runs over the
+whole context (pa_decode_append; the context split across CTAs and merged by
+log-sum-exp). The scatter alone (pa_reshape_and_cache) is timed as a
+component. The default workload is the
 Qwen3-8B-shaped layer: 16 sequences x 4,164 tokens, 32 query / 8 KV heads,
 head_dim 128, bf16, blocks of 16 scattered over a 38,348-block pool.
 
@@ -376,8 +377,12 @@ def run_ours(args, rank, world, local_rank):
 
     def step(i):
         v = views[i % copies]
-        scatter(v)
-        decode(v)
+        if contig:
+            scatter(v)
+            decode(v)
+        else:   # one call: the new tokens written (by the decode kernel itself where it can), then the decode
+            pa.pa_decode_append(v["out"], v["query"], v["key"], v["value"], k_cache, v_cache, v["tables"],
+                                v["lens"], v["max_len"], batch.scale, workspace=workspace)
 
     for i in range(copies):
         step(i)
@@ -526,8 +531,12 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s_e2e, capture_error_mode="thread_local"):
-                pa.pa_reshape_and_cache(sb["k"], sb["v"], k_cache, v_cache, sb["slots"])
-                decode_into(sb["out"], views[c], sb["q"], sb["lens"], sb["tables"])
+                if contig:
+                    pa.pa_reshape_and_cache(sb["k"], sb["v"], k_cache, v_cache, sb["slots"])
+                    decode_into(sb["out"], views[c], sb["q"], sb["lens"], sb["tables"])
+                else:
+                    pa.pa_decode_append(sb["out"], sb["q"], sb["k"], sb["v"], k_cache, v_cache, sb["tables"],
+                                        sb["lens"], views[c]["max_len"], batch.scale, workspace=workspace)
             sb["graphs"].append(g)
         return sb
 
@@ -611,6 +620,8 @@ def run_ours(args, rank, world, local_rank):
     else:
         kernel = "decode_mma_kernel<128,16>"
     decode_launches = plan["kernel_launches"]       # a wide split adds the merge kernel
+    # the per-partition tensor-core kernel writes the step's new tokens itself; other plans scatter first
+    step_launches = decode_launches + (1 if contig or not plan["tensor_cores"] or plan.get("balanced") else 0)
     line = {
         "metric": ("decode attention KV GB/s, contiguous cache (unpaged baseline)" if contig
                    else "paged decode attention KV GB/s (Qwen3-8B shape)" if args.config == "qwen3"
@@ -624,8 +635,8 @@ def run_ours(args, rank, world, local_rank):
                    "graphs": "%d steps per CUDA graph, %d batches alternate" % (GRAPH_STEPS, copies),
                    "l2": "inputs larger than L2: 2 batches of %.0f MB alternate" % (step_kv / 1e6),
                    "plan": plan,
-                   "step": "reshape_and_cache(%d tokens) + %s" % (
-                       nb, "pa_decode_contiguous" if contig else "pa_decode (fused split-K + LSE merge)")},
+                   "step": ("reshape_and_cache(%d tokens) + pa_decode_contiguous" % nb if contig else
+                            "pa_decode_append: %d new tokens into their slots, then the decode" % nb)},
         "tokens_per_s": world * nb / (ms_step * 1e-3),
         "pct_of_8tbs": 100.0 * value / HBM_NOMINAL_GBS,
         "pct_of_measured_hbm": 100.0 * value / peak,
@@ -636,7 +647,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms_step, "steps": e2e_steps},
-        "gpu_launches": (1 + decode_launches) * steps_timed,
+        "gpu_launches": step_launches * steps_timed,
         "components": {"reshape_and_cache_us": scatter_ms * 1e3,
                        "reshape_and_cache_gbs": nb * hkv * d * elem * 2 * 2 / (scatter_ms * 1e-3) / 1e9,
                        "reshape_and_cache_tokens": nb},

@@ -206,22 +206,28 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
                            size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
- * One decode step: pa_reshape_and_cache of the step's new tokens, then
- * pa_decode ([P3] steps 4 and 5: write the new key and value into their
- * slots, then attend over the whole context through the block table).
- * The same two launches, in order, as the two calls; the arguments of both
- * are checked before either is launched, so a refused call writes nothing.
- *   key, value, slot_mapping, num_tokens   as pa_reshape_and_cache
- *   every other argument                   as pa_decode
+ * One decode step ([P3] steps 4 and 5): each sequence's new token is written
+ * into the next slot of its last block -- position context_lens[b] - 1,
+ * its slot found through block_tables -- and then attention runs over the
+ * whole context, new token included. Same result as pa_reshape_and_cache
+ * with those slots followed by pa_decode. The per-partition tensor-core
+ * kernel writes the new tokens itself: the CTA that reads a token's tile
+ * stores the token first (no scatter launch). Other plans launch a small
+ * scatter ahead of the decode.
+ *   new_key, new_value  [num_seqs, num_kv_heads, head_dim], the cache's dtype
+ *   every other argument as pa_decode
+ * A sequence with context_len 0, or past max_context_len (or the table's
+ * reach), writes nothing. All arguments are checked before anything is
+ * launched, so a refused call writes nothing.
  * ---------------------------------------------------------------------- */
 PA_API pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
-                                  const void *key, const void *value, const int64_t *slot_mapping,
-                                  int num_tokens, void *k_cache, void *v_cache, pa_dtype kv_dtype,
-                                  const int32_t *block_tables, const int32_t *context_lens,
-                                  int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                                  int block_size, int max_blocks_per_seq, int num_blocks,
-                                  int max_context_len, float scale, void *workspace,
-                                  size_t workspace_bytes, void *stream);
+                                  const void *new_key, const void *new_value, void *k_cache,
+                                  void *v_cache, pa_dtype kv_dtype, const int32_t *block_tables,
+                                  const int32_t *context_lens, int num_seqs, int num_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_context_len,
+                                  float scale, void *workspace, size_t workspace_bytes,
+                                  void *stream);
 
 /* ------------------------------------------------------------------------
  * Decode attention for a batch whose sequences share their leading blocks.

@@ -128,25 +128,21 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, max_cont
                                 _stream(stream)), "pa_decode")
 
 
-def pa_decode_append(out, query, key, value, slot_mapping, k_cache, v_cache, block_tables, context_lens,
+def pa_decode_append(out, query, new_key, new_value, k_cache, v_cache, block_tables, context_lens,
                      max_context_len, scale, workspace=None, stream=None) -> None:
-    """One decode step: :func:`pa_reshape_and_cache` of ``key`` / ``value``
-    into ``slot_mapping``'s slots, then :func:`pa_decode` into ``out``; both
-    calls' arguments are checked before either kernel is launched."""
+    """One decode step: sequence b's new token (``new_key[b]``, ``new_value[b]``,
+    [B, Hkv, D]) is written to position ``context_lens[b] - 1`` through its
+    block table, then :func:`pa_decode` runs into ``out``."""
     nb, bs, hkv, d = _cache_dims(k_cache)
     B, hq, _ = (int(x) for x in query.shape)
-    if slot_mapping.dtype != torch.int64:
-        raise TypeError("slot_mapping must be int64")
-    T = int(slot_mapping.numel())
-    if T and tuple(key.shape) != (T, hkv, d):
-        raise ValueError("key must be [num_tokens, num_kv_heads, head_dim]")
+    if tuple(new_key.shape) != (B, hkv, d) or tuple(new_value.shape) != (B, hkv, d):
+        raise ValueError("new_key / new_value must be [num_seqs, num_kv_heads, head_dim]")
     ws_bytes = int(workspace.numel() * workspace.element_size()) if workspace is not None else 0
-    _check(_lib.load().pa_decode_append(_ptr(out), _dtype(out), _ptr(query), _dtype(query), _ptr(key),
-                                       _ptr(value), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache),
-                                       _dtype(k_cache), _ptr(block_tables), _ptr(context_lens), B, hq, hkv,
-                                       d, bs, int(block_tables.shape[1]), nb, int(max_context_len),
-                                       float(scale), _ptr(workspace), ws_bytes, _stream(stream)),
-           "pa_decode_append")
+    _check(_lib.load().pa_decode_append(_ptr(out), _dtype(out), _ptr(query), _dtype(query), _ptr(new_key),
+                                       _ptr(new_value), _ptr(k_cache), _ptr(v_cache), _dtype(k_cache),
+                                       _ptr(block_tables), _ptr(context_lens), B, hq, hkv, d, bs,
+                                       int(block_tables.shape[1]), nb, int(max_context_len), float(scale),
+                                       _ptr(workspace), ws_bytes, _stream(stream)), "pa_decode_append")
 
 
 def pa_swap_blocks(dst_k, dst_v, src_k, src_v, block_mapping, stream=None) -> None:

@@ -488,7 +488,8 @@ void fill_common(DecodeParams &p, const DecodeShape &s, const void *query, pa_dt
 pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, const void *query,
                          pa_dtype q_dtype, const void *k_cache, const void *v_cache, pa_dtype kv_dtype,
                          const int32_t *block_tables, const int32_t *context_lens, int contig_stride,
-                         float scale, void *workspace, size_t workspace_bytes, void *stream) {
+                         float scale, void *workspace, size_t workspace_bytes, void *stream,
+                         const void *append_key = nullptr, const void *append_value = nullptr) {
     if (!out || !query || !k_cache || !v_cache || !context_lens) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
@@ -511,6 +512,24 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
     p.nsplit = pl.nsplit;
     p.part_tokens = pl.part_tokens;
     p.cluster_merge = pl.cluster ? 1 : 0;
+    if (pl.balanced || (!pl.cluster && pl.nsplit > 1)) {   // refuse before anything is launched
+        const WorkspaceLayout wl = workspace_layout(s, pl);
+        if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+    }
+    if (append_key) {
+        // the step's new tokens: written by the per-partition tensor-core kernel itself (the CTA
+        // that reads each one writes it first), else by a scatter launched ahead of the decode
+        if (pl.mma && !pl.balanced && contig_stride == 0) {
+            p.append_key = append_key;
+            p.append_value = append_value;
+        } else if (launch_append_last(append_key, append_value, const_cast<void *>(k_cache),
+                                      const_cast<void *>(v_cache), block_tables, context_lens, s.num_seqs,
+                                      s.max_blocks, s.block_size, s.num_blocks, s.max_ctx,
+                                      s.num_kv_heads * s.head_dim * element_bytes(kv_dtype),
+                                      as_stream(stream)) != cudaSuccess) {
+            return PA_ERR_CUDA;
+        }
+    }
     if (pl.balanced) {
         const WorkspaceLayout wl = workspace_layout(s, pl);
         if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
@@ -687,29 +706,22 @@ PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, void *
 }
 
 PA_API pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
-                                  const void *key, const void *value, const int64_t *slot_mapping,
-                                  int num_tokens, void *k_cache, void *v_cache, pa_dtype kv_dtype,
-                                  const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
-                                  int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                  const void *new_key, const void *new_value, void *k_cache, void *v_cache,
+                                  pa_dtype kv_dtype, const int32_t *block_tables, const int32_t *context_lens,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                                   int max_blocks_per_seq, int num_blocks, int max_context_len, float scale,
                                   void *workspace, size_t workspace_bytes, void *stream) {
-    // every check of both calls first, so that a refused call launches nothing
     const DecodeShape s{num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                         max_blocks_per_seq, num_blocks, max_context_len};
     pa_status st = check_shape(s);
     if (st != PA_OK) return st;
     if (!valid_dtype(out_dtype) || !std::isfinite(scale)) return PA_ERR_INVALID_ARG;
     if ((st = check_dtypes(q_dtype, kv_dtype)) != PA_OK) return st;
-    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
-    if (num_tokens > 0 && (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value)))
-        return PA_ERR_INVALID_ARG;
-    if (num_seqs > 0 && !block_tables) return PA_ERR_INVALID_ARG;
-    if ((st = pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, num_blocks,
-                                   block_size, num_kv_heads, head_dim, kv_dtype, stream)) != PA_OK)
-        return st;
     if (num_seqs == 0) return PA_OK;
+    if (!block_tables || !new_key || !new_value || !aligned16(new_key) || !aligned16(new_value))
+        return PA_ERR_INVALID_ARG;
     return decode_planned(s, out, out_dtype, query, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
-                          context_lens, 0, scale, workspace, workspace_bytes, stream);
+                          context_lens, 0, scale, workspace, workspace_bytes, stream, new_key, new_value);
 }
 
 PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,

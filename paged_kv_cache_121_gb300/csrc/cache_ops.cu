@@ -61,6 +61,44 @@ cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k
                          num_slots, row_vecs);
 }
 
+// The step's new token of every sequence, written to position
+// context_lens[b] - 1 (its slot taken from the block table): the scatter of
+// pa_decode_append where the decode kernel does not write it itself. One CTA
+// per sequence; lengths of 0, or past len_cap, write nothing.
+__global__ void __launch_bounds__(128)
+append_last_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value, uint4 *__restrict__ k_cache,
+                   uint4 *__restrict__ v_cache, const int32_t *__restrict__ block_tables,
+                   const int32_t *__restrict__ context_lens, int max_blocks, int block_size, int num_blocks,
+                   int len_cap, int row_vecs) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+    const int b = blockIdx.x;
+    const int len = context_lens[b];
+    if (len <= 0 || len > len_cap || len > max_blocks * block_size) return;
+    const int pos = len - 1;
+    const int blk = block_tables[static_cast<int64_t>(b) * max_blocks + pos / block_size];
+    if (blk < 0 || blk >= num_blocks) return;
+    const int64_t slot = static_cast<int64_t>(blk) * block_size + pos % block_size;
+    for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
+        const uint4 a = key[static_cast<int64_t>(b) * row_vecs + c];
+        const uint4 v = value[static_cast<int64_t>(b) * row_vecs + c];
+        k_cache[slot * row_vecs + c] = a;
+        v_cache[slot * row_vecs + c] = v;
+    }
+}
+
+cudaError_t launch_append_last(const void *key, const void *value, void *k_cache, void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                               int max_blocks, int block_size, int num_blocks, int len_cap, int row_bytes,
+                               cudaStream_t stream) {
+    const int row_vecs = row_bytes / 16;
+    const int threads = row_vecs >= 128 ? 128 : ((row_vecs + 31) / 32) * 32;
+    return launch_kernel(append_last_kernel, dim3(num_seqs), dim3(threads), 0, stream, 1u,
+                         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value),
+                         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), block_tables,
+                         context_lens, max_blocks, block_size, num_blocks, len_cap, row_vecs);
+}
+
 constexpr int kCopyChunkVecs = 512;  // 8 KiB per CTA
 
 __global__ void __launch_bounds__(256)

@@ -55,6 +55,8 @@ struct DecodeParams {
     int out_f16;
     int q_bf16;
     int kv_f16;          // 16-bit query and caches are fp16 (else bf16)
+    const void *append_key;     // [num_seqs, Hkv, D] or null: the step's new token of sequence b,
+    const void *append_value;   //   written to position context_lens[b] - 1 before it is read
     float scale_log2;    // scale * log2(e): scores are kept in base-2 units
 };
 

@@ -48,6 +48,10 @@ size_t decode_balanced_smem_extra(int num_seqs);
 cudaError_t launch_decode_balanced(const DecodeParams &p, const BalancedParams &bp, const CUtensorMap &tmap_k,
                                    const CUtensorMap &tmap_v, dim3 grid, cudaStream_t stream);
 cudaError_t launch_balanced_merge(const DecodeParams &p, const BalancedParams &bp, cudaStream_t stream);
+cudaError_t launch_append_last(const void *key, const void *value, void *k_cache, void *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                               int max_blocks, int block_size, int num_blocks, int len_cap, int row_bytes,
+                               cudaStream_t stream);
 // kv_type / out_type: 0 fp32, 1 bf16, 2 fp16 (the public dtype codes)
 cudaError_t launch_decode_simt(const DecodeParams &p, int kv_type, dim3 grid, cudaStream_t stream);
 cudaError_t launch_lse_merge(void *out, int out_type, const float *tmp_out, const float *max_logits,

@@ -1,9 +1,12 @@
-"""pa_decode_append: the step's scatter and decode in one call ("PagedAttention,
-explained.", procedure steps 4 and 5). The result must be the oracle's
-(scatter, then attention over the updated cache) and bit-for-bit the result
-of the two calls made separately, on every decode path: cluster and
-per-partition, each load mode, the wide split with its merge kernel, the
-ragged-balanced path, fp16; a refused call writes nothing."""
+"""pa_decode_append: one decode step ("PagedAttention, explained.", procedure
+steps 4 and 5) -- each sequence's new token written to position
+context_len - 1, then attention over the whole context. The per-partition
+tensor-core kernel writes the token itself (the CTA that reads its tile
+stores it first); other plans scatter ahead. The result must be the
+oracle's (scatter, then attention over the updated cache), the caches bit
+for bit, and bit for bit the result of pa_reshape_and_cache + pa_decode, on
+every path: cluster and workspace splits, each load mode, the CUDA-core
+kernel, the ragged-balanced path, fp16; a refused call writes nothing."""
 import numpy as np
 import pytest
 import torch
@@ -27,9 +30,8 @@ CASES = [
 
 def run_append(db, ws, out_dtype=torch.float32):
     b = db.h
-    slots = torch.from_numpy(new_token_slots(b)).cuda()
     out = torch.empty((b.num_seqs, b.num_heads, b.head_dim), dtype=out_dtype, device="cuda")
-    pa.pa_decode_append(out, db.query, db.new_key, db.new_value, slots, db.k_cache, db.v_cache, db.block_tables,
+    pa.pa_decode_append(out, db.query, db.new_key, db.new_value, db.k_cache, db.v_cache, db.block_tables,
                         db.context_lens, b.max_context_len, b.scale, workspace=ws)
     return out
 
@@ -77,19 +79,18 @@ def test_append_balanced_and_in_a_graph():
     assert pa.pa_decode_plan(160, 32, 8, 128, 16, int(lens.max()), with_workspace=True)["balanced"]
     db = DeviceBatch(batch)
     ws = make_workspace(batch)
-    slots = torch.from_numpy(new_token_slots(batch)).cuda()
     out = torch.empty((160, 32, 128), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        pa.pa_decode_append(out, db.query, db.new_key, db.new_value, slots, db.k_cache, db.v_cache,
+        pa.pa_decode_append(out, db.query, db.new_key, db.new_value, db.k_cache, db.v_cache,
                             db.block_tables, db.context_lens, batch.max_context_len, batch.scale, workspace=ws)
     torch.cuda.synchronize()
     want, _, _ = oracle_step(batch)
     assert max_err(out, want) <= ATOL
     # captured and replayed: the scatter rewrites the same values, the decode gives the same output
     with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-        pa.pa_decode_append(out, db.query, db.new_key, db.new_value, slots, db.k_cache, db.v_cache,
+        pa.pa_decode_append(out, db.query, db.new_key, db.new_value, db.k_cache, db.v_cache,
                             db.block_tables, db.context_lens, batch.max_context_len, batch.scale, workspace=ws)
     out.zero_()
     for _ in range(3):
@@ -105,13 +106,25 @@ def test_append_refuses_before_launching():
     batch = workloads.make_batch("append_bad", (10, 20), 8, 2, 128, 16, 8, True, seed_values=960)
     db = DeviceBatch(batch)
     before = bits(db.k_cache).copy()
-    slots = torch.from_numpy(new_token_slots(batch)).cuda()
     out = torch.empty((2, 8, 128), dtype=torch.float32, device="cuda")
-    status = pa.load_library().pa_decode_append(
-        out.data_ptr(), pa.PA_F32, db.query.data_ptr(), pa.PA_BF16, db.new_key.data_ptr(), db.new_value.data_ptr(),
-        slots.data_ptr(), 2, db.k_cache.data_ptr(), db.v_cache.data_ptr(), pa.PA_BF16, db.block_tables.data_ptr(),
-        db.context_lens.data_ptr(), 2, 8, 3, 128, 16, int(db.block_tables.shape[1]), 8, 20, 0.1, None, 0,
-        torch.cuda.current_stream().cuda_stream)
-    assert status == pa.PA_ERR_INVALID_ARG
+    lib = pa.load_library()
+    args = [out.data_ptr(), pa.PA_F32, db.query.data_ptr(), pa.PA_BF16, db.new_key.data_ptr(),
+            db.new_value.data_ptr(), db.k_cache.data_ptr(), db.v_cache.data_ptr(), pa.PA_BF16,
+            db.block_tables.data_ptr(), db.context_lens.data_ptr(), 2, 8, 3, 128, 16,
+            int(db.block_tables.shape[1]), 8, 20, 0.1, None, 0, torch.cuda.current_stream().cuda_stream]
+    assert lib.pa_decode_append(*args) == pa.PA_ERR_INVALID_ARG
+    # a split that needs a workspace, called with a null one: refused, nothing written either
+    long_batch = workloads.make_batch("append_ws", (3000, 4000), 16, 4, 128, 16, 450, True, seed_values=961)
+    ldb = DeviceBatch(long_batch)
+    lbefore = bits(ldb.k_cache).copy()
+    lout = torch.empty((2, 16, 128), dtype=torch.float32, device="cuda")
+    assert not pa.pa_decode_plan(2, 16, 4, 128, 16, 4000, with_workspace=True)["cluster_merge"]
+    status = lib.pa_decode_append(lout.data_ptr(), pa.PA_F32, ldb.query.data_ptr(), pa.PA_BF16,
+                                  ldb.new_key.data_ptr(), ldb.new_value.data_ptr(), ldb.k_cache.data_ptr(),
+                                  ldb.v_cache.data_ptr(), pa.PA_BF16, ldb.block_tables.data_ptr(),
+                                  ldb.context_lens.data_ptr(), 2, 16, 4, 128, 16, int(ldb.block_tables.shape[1]),
+                                  450, 4000, 0.1, None, 1, torch.cuda.current_stream().cuda_stream)
+    assert status == pa.PA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert np.array_equal(bits(db.k_cache), before)
+    assert np.array_equal(bits(ldb.k_cache), lbefore)

@@ -620,8 +620,8 @@ def run_ours(args, rank, world, local_rank):
     else:
         kernel = "decode_mma_kernel<128,16>"
     decode_launches = plan["kernel_launches"]       # a wide split adds the merge kernel
-    # the per-partition tensor-core kernel writes the step's new tokens itself; other plans scatter first
-    step_launches = decode_launches + (1 if contig or not plan["tensor_cores"] or plan.get("balanced") else 0)
+    # the tensor-core kernels write the step's new tokens themselves; the CUDA-core one scatters first
+    step_launches = decode_launches + (1 if contig or not plan["tensor_cores"] else 0)
     line = {
         "metric": ("decode attention KV GB/s, contiguous cache (unpaged baseline)" if contig
                    else "paged decode attention KV GB/s (Qwen3-8B shape)" if args.config == "qwen3"

@@ -216,9 +216,11 @@ PA_API pa_status pa_decode(void *out, pa_dtype out_dtype, const void *query, pa_
  * scatter ahead of the decode.
  *   new_key, new_value  [num_seqs, num_kv_heads, head_dim], the cache's dtype
  *   every other argument as pa_decode
- * A sequence with context_len 0, or past max_context_len (or the table's
- * reach), writes nothing. All arguments are checked before anything is
- * launched, so a refused call writes nothing.
+ * A sequence with context_len 0 writes nothing; so does one whose length
+ * the decode cuts short (past the table's reach; a length past
+ * max_context_len breaks the call's contract, as for pa_decode). All
+ * arguments are checked before anything is launched, so a refused call
+ * writes nothing.
  * ---------------------------------------------------------------------- */
 PA_API pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *query, pa_dtype q_dtype,
                                   const void *new_key, const void *new_value, void *k_cache,

@@ -517,9 +517,9 @@ pa_status decode_planned(const DecodeShape &s, void *out, pa_dtype out_dtype, co
         if (!workspace || workspace_bytes < wl.total || !aligned16(workspace)) return PA_ERR_WORKSPACE;
     }
     if (append_key) {
-        // the step's new tokens: written by the per-partition tensor-core kernel itself (the CTA
-        // that reads each one writes it first), else by a scatter launched ahead of the decode
-        if (pl.mma && !pl.balanced && contig_stride == 0) {
+        // the step's new tokens: written by the tensor-core kernels themselves (the CTA that
+        // reads each one writes it first), else by a scatter launched ahead of the decode
+        if (pl.mma && contig_stride == 0) {
             p.append_key = append_key;
             p.append_value = append_value;
         } else if (launch_append_last(append_key, append_value, const_cast<void *>(k_cache),

@@ -195,37 +195,49 @@ decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
         // ------------------------------ producer ------------------------------
         // Lane l holds the block id and the in-block token offset of tile
         // start + 32 k + l for the current chunk k, the next chunk fetched
-        // ahead. Tiles past the range are not looked up.
+        // ahead, and (when the step's new tokens are written here) the
+        // sequence whose last tile it is, else -1. Tiles past the range are
+        // not looked up.
         uint64_t policy = 0;
         if (lane == 0) {
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
             policy = l2_policy_evict_first();
         }
-        auto lookup = [&](int i, int &blk, int &off) {
+        auto lookup = [&](int i, int &blk, int &off, int &last_of) {
             blk = 0;
             off = 0;
+            last_of = -1;
             if (i < ntiles) {
                 const int g = start + i;
                 const int b = seq_of(P, B, g);
                 const int tok = (g - P[b]) * kTT;
                 blk = p.block_tables[static_cast<int64_t>(b) * p.max_blocks + tok / bs];
                 off = tok % bs;
+                if (p.append_key && g == P[b + 1] - 1 && p.context_lens[b] == attended_len(p, bp, b))
+                    last_of = b;   // a length cut short writes none
             }
         };
-        int cur_blk, cur_off, nxt_blk, nxt_off;
-        lookup(lane, cur_blk, cur_off);
-        lookup(32 + lane, nxt_blk, nxt_off);
         const int head0 = hgrp * hpc;
+        int cur_blk, cur_off, cur_last, nxt_blk, nxt_off, nxt_last;
+        lookup(lane, cur_blk, cur_off, cur_last);
+        lookup(32 + lane, nxt_blk, nxt_off, nxt_last);
         int issued = 0;
         for (int i = 0; i < ntiles; ++i) {
             if ((i & 31) == 0 && i > 0) {
                 cur_blk = nxt_blk;
                 cur_off = nxt_off;
-                lookup(i + 32 + lane, nxt_blk, nxt_off);
+                cur_last = nxt_last;
+                lookup(i + 32 + lane, nxt_blk, nxt_off, nxt_last);
             }
             const int blk = __shfl_sync(0xffffffffu, cur_blk, i & 31);
             const int off = __shfl_sync(0xffffffffu, cur_off, i & 31);
+            const int last_of = __shfl_sync(0xffffffffu, cur_last, i & 31);
+            if (last_of >= 0) {   // the tile holds a sequence's new token: store it before reading the tile
+                const int pos = attended_len(p, bp, last_of) - 1;
+                warp_append_row<D>(p, p.append_key, p.k_cache, last_of, pos, head0, hpc, lane);
+                warp_append_row<D>(p, p.append_value, p.v_cache, last_of, pos, head0, hpc, lane);
+            }
             int ok = 1;
             if (lane == 0) {
                 const int s = i % nstages, k = i / nstages;

@@ -68,27 +68,6 @@ __device__ __forceinline__ void store_out2(const DecodeParams &p, int64_t idx, f
 
 // Write a warp's result (final output or split-K partition) for query heads
 // h0 .. h0+rows-1.
-// The step's new token of sequence b (position pos), heads head0 ..
-// head0+hpc-1 of K (or V), copied by one warp into its slot of the cache,
-// then made visible to this CTA's later TMA / bulk reads of that slot (the
-// generic-proxy writes are fenced against the async proxy before the warp
-// moves on). "PagedAttention, explained.", procedure step 4.
-template <int D>
-__device__ __forceinline__ void warp_append_row(const DecodeParams &p, const void *src_rows, const void *cache,
-                                                int b, int pos, int head0, int hpc, int lane) {
-    const int blk = p.block_tables[static_cast<int64_t>(b) * p.max_blocks + pos / p.block_size];
-    if (static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks)) {
-        const int64_t slot = static_cast<int64_t>(blk) * p.block_size + pos % p.block_size;
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            static_cast<const uint16_t *>(src_rows) + (static_cast<int64_t>(b) * p.num_kv_heads + head0) * D);
-        uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(static_cast<const uint16_t *>(cache)) +
-                                               (slot * p.num_kv_heads + head0) * D);
-        for (int c = lane; c < hpc * D / 8; c += 32) dst[c] = src[c];
-    }
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    __syncwarp();
-}
-
 template <int D>
 __device__ __forceinline__ void warp_epilogue(const DecodeParams &p, WarpState<D> &st, int b, int part,
                                               int h0, int rows, int lane) {
@@ -319,7 +298,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const unsigned char *src_base = static_cast<const unsigned char *>(is_v ? p.v_cache : p.k_cache) +
                                         hgrp * hpc * D * 2 + (t & (bs - 1)) * row_bytes;
         const uint32_t dst_lane = static_cast<uint32_t>((is_v ? v_off : 0) + t * row_pitch);
-        if (p.append_key && tok_begin <= w.len - 1 && w.len - 1 < tok_end)   // this CTA reads the new token
+        if (p.append_key && tok_begin <= w.len - 1 && w.len - 1 < tok_end &&
+            p.context_lens[b] == w.len)   // this CTA reads the new token (a length cut short writes none)
             warp_append_row<D>(p, is_v ? p.append_value : p.append_key, is_v ? p.v_cache : p.k_cache, b,
                                w.len - 1, hgrp * hpc, hpc, lane);
         int issued = 0;
@@ -385,7 +365,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         int nxt0 = entry(32 + lane, 0), nxt1 = kPairs ? entry(32 + lane, 1) : 0;
         int issued = 0;
         const int head0 = hgrp * hpc;
-        if (p.append_key && tok_begin <= w.len - 1 && w.len - 1 < tok_end) {   // this CTA reads the new token
+        if (p.append_key && tok_begin <= w.len - 1 && w.len - 1 < tok_end &&
+            p.context_lens[b] == w.len) {   // this CTA reads the new token (a length cut short writes none)
             warp_append_row<D>(p, p.append_key, p.k_cache, b, w.len - 1, head0, hpc, lane);
             warp_append_row<D>(p, p.append_value, p.v_cache, b, w.len - 1, head0, hpc, lane);
         }

@@ -81,6 +81,27 @@ __device__ __forceinline__ void load_query_fragments(uint32_t (&qa)[D / 16][4], 
     }
 }
 
+// The step's new token of sequence b (position pos), heads head0 ..
+// head0+hpc-1 of K (or V), copied by one warp into its slot of the cache,
+// then made visible to this CTA's later TMA / bulk reads of that slot (the
+// generic-proxy writes are fenced against the async proxy before the warp
+// moves on). "PagedAttention, explained.", procedure step 4.
+template <int D>
+__device__ __forceinline__ void warp_append_row(const DecodeParams &p, const void *src_rows, const void *cache,
+                                                int b, int pos, int head0, int hpc, int lane) {
+    const int blk = p.block_tables[static_cast<int64_t>(b) * p.max_blocks + pos / p.block_size];
+    if (static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks)) {
+        const int64_t slot = static_cast<int64_t>(blk) * p.block_size + pos % p.block_size;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const uint16_t *>(src_rows) + (static_cast<int64_t>(b) * p.num_kv_heads + head0) * D);
+        uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(static_cast<const uint16_t *>(cache)) +
+                                               (slot * p.num_kv_heads + head0) * D);
+        for (int c = lane; c < hpc * D / 8; c += 32) dst[c] = src[c];
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+}
+
 // S = Q K^T for the tile, masking, online softmax update, O += P V. Tokens at
 // or past valid0 (row r) / valid1 (row r + 8) get score -inf. V rows of tokens
 // past the tile's data must already hold zeros (0 * NaN would leak).

@@ -24,7 +24,8 @@ CASES = [
     ((3000, 4000), 16, 4, 128, 16, False, True),                   # wide split + merge kernel
     ((1, 7, 8, 9, 64, 250), 16, 4, 128, 8, False, True),           # two blocks per tile
     ((19, 90, 300), 8, 2, 128, 4, True, True),                     # bulk row copies, fp16
-    ((40, 90), 8, 2, 64, 12, False, True),                         # CUDA-core kernel
+    ((40, 90), 8, 2, 64, 12, False, True),                         # CUDA-core kernel: scatter launched first
+    ((0, 5, 33, 0, 200, 16), 16, 4, 128, 32, False, False),         # empty sequences write nothing
 ]
 
 
@@ -56,6 +57,7 @@ def test_append_matches_oracle_and_separate_calls(case):
     need = sum(workloads.cdiv(n, bs) for n in lens)
     batch = workloads.make_batch("append", lens, hq, hkv, d, bs, need + 9, not f16, seed_values=900 + case,
                                  f16=f16)
+    batch.new_pos = np.array([n - 1 if n > 0 else -1 for n in lens], np.int32)   # the new token: position len - 1
     db = DeviceBatch(batch)
     ws = make_workspace(batch) if use_ws else None
     out = run_append(db, ws)

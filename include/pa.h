@@ -8,9 +8,9 @@
  * surface at the caller's next synchronisation, as usual in CUDA.
  *
  * Conventions shared by every entry point
- *  - Pointers named *_cache, query, key, value, out, block_tables,
- *    context_lens, slot_mapping, block_mapping, tmp_out, max_logits,
- *    exp_sums and workspace are caller-owned DEVICE memory, contiguous,
+ *  - Pointers named *_cache, query, key, value, new_key, new_value, out,
+ *    block_tables, context_lens, slot_mapping, block_mapping, tmp_out,
+ *    max_logits, exp_sums and workspace are caller-owned DEVICE memory, contiguous,
  *    row-major, 16-byte aligned. The library keeps no reference after the
  *    call returns.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default

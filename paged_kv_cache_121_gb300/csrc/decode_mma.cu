@@ -19,7 +19,12 @@
 //    [num_blocks, block_size, Hkv, D] layout -- is fetched as one burst, and
 //    the producer issues two instructions per tile. Rows land head by head
 //    as 64-dim halves with the 128-byte swizzle, which makes the matrix loads
-//    below bank-conflict free.
+//    below bank-conflict free. Blocks of 1, 2 or 4 tokens are gathered row
+//    by row with bulk copies instead (rows mode, below).
+//  * Called for a decode step (pa_decode_append), the producer of the CTA
+//    whose partition holds a sequence's newest token first stores that
+//    token's K and V rows into their slot ("PagedAttention, explained.",
+//    procedure step 4), fenced against the async proxy that reads them.
 //  * Consumer warp j owns KV head j of the group for the whole CTA and reads
 //    every stage. S = Q K^T runs on the tensor cores (mma.m16n8k16, M = the
 //    query heads of the GQA group, N = tokens, K = head dims; Q stays in

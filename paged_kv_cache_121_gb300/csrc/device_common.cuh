@@ -1,7 +1,7 @@
 // Device-side building blocks shared by the decode kernels: parameter block,
-// PTX wrappers (mbarrier, TMA, ldmatrix, mma), bounded waits, and the CTA
-// epilogue that either writes the final output, writes split-K partitions,
-// or merges partitions in the last CTA to finish (log-sum-exp).
+// PTX wrappers (mbarrier, TMA and bulk copies, ldmatrix, mma), bounded waits,
+// programmatic dependent launch, and the CUDA-core kernel's CTA epilogue,
+// which writes either the final output or a split-K partition.
 #pragma once
 
 #include <cuda.h>

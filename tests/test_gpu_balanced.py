@@ -27,10 +27,10 @@ from gpu_cases import ATOL, DeviceBatch, make_workspace, max_err, oracle_step, r
 pytestmark = pytest.mark.gpu
 
 
-def ragged_batch(name, lens, hq, hkv, d, bs, seed):
+def ragged_batch(name, lens, hq, hkv, d, bs, seed, max_blocks=None):
     need = sum(workloads.cdiv(int(n), bs) for n in lens)
     return workloads.make_batch(name, lens, hq, hkv, d, bs, need + 11, True, seed_values=seed,
-                                seed_blocks=seed + 1)
+                                seed_blocks=seed + 1, max_blocks=max_blocks)
 
 
 @pytest.mark.parametrize("case", [
@@ -52,7 +52,9 @@ def test_balanced_is_chosen_for_many_sequences(case, out_dtype):
     plan = pa.pa_decode_plan(B, hq, hkv, d, bs, int(lens.max()), pa.PA_BF16, with_workspace=True)
     assert plan["balanced"] == 1 and plan["kernel_launches"] == 2
     db = DeviceBatch(batch)
-    out = run_step(db, workspace=make_workspace(batch), out_dtype=out_dtype)
+    ws = make_workspace(batch)
+    ws.copy_(torch.randint(0, 256, ws.shape, dtype=torch.uint8, device="cuda"))   # needs no initialisation
+    out = run_step(db, workspace=ws, out_dtype=out_dtype)
     want, _, _ = oracle_step(batch)
     g = out.float().cpu().numpy().astype(np.float64)
     tol = ATOL + (np.abs(want) * 2.0 ** -8 if out_dtype == torch.bfloat16 else 0.0)
@@ -80,6 +82,7 @@ FORCED = [
     ((400, 333, 250), 24, 12, 64, 16, None),            # 12 KV heads: groups of 6
     ((900, 100, 650), 8, 2, 128, 128, 600),             # lengths past the host bound are cut
     ((1,) * 40 + (4000,), 16, 4, 128, 16, None),        # one long sequence among many short
+    ((0, 0, 0), 8, 2, 128, 16, 64),                     # no tile at all: zeros only
 ]
 
 
@@ -87,19 +90,24 @@ def child_main():
     results = []
     for i, (lens, hq, hkv, d, bs, mcl) in enumerate(FORCED):
         lens = np.asarray(lens, np.int32)
-        batch = ragged_batch("forced", lens, hq, hkv, d, bs, seed=300 + i)
+        batch = ragged_batch("forced", lens, hq, hkv, d, bs, seed=300 + i,
+                             max_blocks=None if lens.max() > 0 else workloads.cdiv(mcl, bs))
         batch.new_pos = np.full(len(lens), -1, np.int32)
         bound = int(lens.max()) if mcl is None else mcl
         plan = pa.pa_decode_plan(len(lens), hq, hkv, d, bs, bound, pa.PA_BF16, with_workspace=True)
         db = DeviceBatch(batch)
         ws = make_workspace(batch, max_context_len=bound)
-        out = torch.full((len(lens), hq, d), 5.0, dtype=torch.float32, device="cuda")
-        pa.pa_decode(out, db.query, db.k_cache, db.v_cache, db.block_tables, db.context_lens, bound,
-                     batch.scale, workspace=ws)
+        ws.fill_(0xFF)   # the workspace needs no initialisation
         want = oracle.paged_attention(batch.query, batch.k_cache, batch.v_cache, batch.block_tables,
                                       np.minimum(lens, bound), batch.scale)
+        errs = []
+        for _ in range(3):   # the same workspace again: nothing left by one call leaks into the next
+            out = torch.full((len(lens), hq, d), 5.0, dtype=torch.float32, device="cuda")
+            pa.pa_decode(out, db.query, db.k_cache, db.v_cache, db.block_tables, db.context_lens, bound,
+                         batch.scale, workspace=ws)
+            errs.append(max_err(out, want))
         torch.cuda.synchronize()
-        results.append({"case": i, "balanced": plan["balanced"], "err": max_err(out, want),
+        results.append({"case": i, "balanced": plan["balanced"], "err": max(errs),
                         "status": pa.pa_device_status(clear=True)})
     print(json.dumps(results))
 

@@ -93,6 +93,49 @@ __device__ __forceinline__ int cta_of(int t, int W, int C) {
     return static_cast<int>((static_cast<int64_t>(t + 1) * C - 1) / W);
 }
 
+// The step's new token of sequence b (position pos, in block blk: the block
+// of the tile being loaded) for heads head0 .. head0+hpc-1, K and V, copied
+// by one warp into its slot, then fenced against the async proxy so that the
+// TMA reads of the tile that follow see it ("PagedAttention, explained.",
+// procedure step 4). The block id comes from the producer's lookup and both
+// rows are loaded before either is stored: one round trip to memory instead
+// of a table read and a row read for each of K and V, in the middle of the
+// pipeline.
+template <int D>
+__device__ __forceinline__ void append_kv(const DecodeParams &p, int blk, int b, int pos, int head0, int hpc,
+                                          int lane) {
+    constexpr int kPer = kMaxHeads * D / 8 / 32;   // 16-byte pieces per lane and row, at most
+    const int n = hpc * D / 8;
+    if (static_cast<unsigned>(blk) < static_cast<unsigned>(p.num_blocks)) {
+        const int64_t src_off = (static_cast<int64_t>(b) * p.num_kv_heads + head0) * D;
+        const int64_t slot = static_cast<int64_t>(blk) * p.block_size + pos % p.block_size;
+        const int64_t dst_off = (slot * p.num_kv_heads + head0) * D;
+        const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.append_key) + src_off);
+        const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.append_value) + src_off);
+        uint4 *kd = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(static_cast<const uint16_t *>(p.k_cache)) + dst_off);
+        uint4 *vd = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(static_cast<const uint16_t *>(p.v_cache)) + dst_off);
+        uint4 kr[kPer], vr[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int c = lane + 32 * j;
+            if (c < n) {
+                kr[j] = ks[c];
+                vr[j] = vs[c];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int c = lane + 32 * j;
+            if (c < n) {
+                kd[c] = kr[j];
+                vd[c] = vr[j];
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+}
+
 __device__ __forceinline__ void prefetch_l1(const void *ptr) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
 }
@@ -233,11 +276,8 @@ decode_balanced_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_
             const int blk = __shfl_sync(0xffffffffu, cur_blk, i & 31);
             const int off = __shfl_sync(0xffffffffu, cur_off, i & 31);
             const int last_of = __shfl_sync(0xffffffffu, cur_last, i & 31);
-            if (last_of >= 0) {   // the tile holds a sequence's new token: store it before reading the tile
-                const int pos = attended_len(p, bp, last_of) - 1;
-                warp_append_row<D>(p, p.append_key, p.k_cache, last_of, pos, head0, hpc, lane);
-                warp_append_row<D>(p, p.append_value, p.v_cache, last_of, pos, head0, hpc, lane);
-            }
+            if (last_of >= 0)   // the tile holds a sequence's new token: store it before reading the tile
+                append_kv<D>(p, blk, last_of, attended_len(p, bp, last_of) - 1, head0, hpc, lane);
             int ok = 1;
             if (lane == 0) {
                 const int s = i % nstages, k = i / nstages;

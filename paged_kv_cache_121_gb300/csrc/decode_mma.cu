@@ -114,14 +114,18 @@ __device__ __forceinline__ void warp_epilogue(const DecodeParams &p, WarpState<D
 // Split merged inside a thread-block cluster: the cluster is the nsplit
 // partitions of one (sequence, KV-head group, head tile). Each CTA leaves the
 // per-head softmax states of its partition in its own shared memory (m[16],
-// l[16], O[16][D] per head); after a cluster barrier every CTA merges a slice
-// of the outputs by reading all partitions straight from its peers' shared
-// memory; a second barrier keeps each CTA (and its shared memory) alive until
-// every peer is done reading it. No global workspace, no atomics.
+// l[16], O[16][D + 8] per head: rows padded by 8 floats, so that the 8-byte
+// stores of a half-warp's four rows fall in 32 different banks); after a
+// cluster barrier every CTA merges a slice of the outputs by reading all
+// partitions straight from its peers' shared memory; a second barrier keeps
+// each CTA (and its shared memory) alive until every peer is done reading it.
+// Its arrive is relaxed: the reads it waits for have been consumed by then,
+// and nothing else needs ordering. No global workspace, no atomics.
 template <int D>
 __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, const WarpState<D> &st, float *sm, int b,
                                        int hgrp, int tile, int rows, int warp, int lane) {
-    constexpr int kRegion = 32 + kRowsPerTile * D;   // floats per head
+    constexpr int kStride = D + 8;                         // floats per state row
+    constexpr int kRegion = 32 + kRowsPerTile * kStride;   // floats per head
     const int hpc = p.heads_per_cta;
     if (warp < hpc) {
         float *reg = sm + warp * kRegion;
@@ -129,8 +133,8 @@ __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, co
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn) {
             const int d = 8 * dn + 2 * q4;
-            *reinterpret_cast<float2 *>(reg + 32 + r * D + d) = make_float2(st.o[dn][0], st.o[dn][1]);
-            *reinterpret_cast<float2 *>(reg + 32 + (r + 8) * D + d) = make_float2(st.o[dn][2], st.o[dn][3]);
+            *reinterpret_cast<float2 *>(reg + 32 + r * kStride + d) = make_float2(st.o[dn][0], st.o[dn][1]);
+            *reinterpret_cast<float2 *>(reg + 32 + (r + 8) * kStride + d) = make_float2(st.o[dn][2], st.o[dn][3]);
         }
         if (q4 == 0) {   // (max, sum) pairs, row-major
             *reinterpret_cast<float2 *>(reg + 2 * r) = make_float2(st.m0, st.l0);
@@ -156,7 +160,7 @@ __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, co
         const int rem = idx - j * rows * kD4;
         const int rr = rem / kD4, d4 = rem - rr * kD4;
         const uint32_t ml_off = base + 4u * static_cast<uint32_t>(j * kRegion + 2 * rr);
-        const uint32_t o_off = base + 4u * static_cast<uint32_t>(j * kRegion + 32 + rr * D + 4 * d4);
+        const uint32_t o_off = base + 4u * static_cast<uint32_t>(j * kRegion + 32 + rr * kStride + 4 * d4);
         float2 ml[8];
         float4 oq[8];
 #pragma unroll
@@ -191,7 +195,8 @@ __device__ __forceinline__ void cluster_exchange_merge(const DecodeParams &p, co
         store_out2(p, o, acc.x * inv, acc.y * inv);
         store_out2(p, o + 2, acc.z * inv, acc.w * inv);
     }
-    cluster_sync_all();   // peers have finished reading this CTA's shared memory
+    // peers have finished reading this CTA's shared memory
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // How the producer fills a stage: one TMA box per tile (blocks of 16 tokens
@@ -534,7 +539,7 @@ int decode_mma_ring_bytes(int head_dim, int block_size, int heads_per_cta, int b
 }
 
 int decode_mma_cluster_bytes(int head_dim, int heads_per_cta) {
-    return heads_per_cta * (32 + kRowsPerTile * head_dim) * 4;
+    return heads_per_cta * (32 + kRowsPerTile * (head_dim + 8)) * 4;   // the exchange's state rows, padded
 }
 
 int decode_mma_load_mode(int block_size, bool contiguous) {

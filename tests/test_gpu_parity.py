@@ -46,6 +46,8 @@ SMALL = [
     ((33, 200, 17), 24, 12, 128, 16, True),        # 12 KV heads: groups of 6 per CTA
     ((70, 300), 32, 16, 64, 32, True),             # 16 KV heads: two groups of 8
     ((5, 600), 12, 3, 128, 128, True),             # large blocks: 8 tiles per block
+    ((5, 700), 8, 2, 128, 256, True),              # the largest blocks: tiles at offsets up to 240
+    ((3, 513), 64, 1, 64, 256, True),              # G = 64: four head tiles over one KV head
 ]
 
 

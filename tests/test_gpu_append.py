@@ -26,6 +26,7 @@ CASES = [
     ((19, 90, 300), 8, 2, 128, 4, True, True),                     # bulk row copies, fp16
     ((40, 90), 8, 2, 64, 12, False, True),                         # CUDA-core kernel: scatter launched first
     ((0, 5, 33, 0, 200, 16), 16, 4, 128, 32, False, False),         # empty sequences write nothing
+    ((1, 255, 256, 257, 600), 8, 2, 128, 256, False, True),          # new tokens on both sides of a 256-token block boundary
 ]
 
 

@@ -83,6 +83,7 @@ FORCED = [
     ((900, 100, 650), 8, 2, 128, 128, 600),             # lengths past the host bound are cut
     ((1,) * 40 + (4000,), 16, 4, 128, 16, None),        # one long sequence among many short
     ((0, 0, 0), 8, 2, 128, 16, 64),                     # no tile at all: zeros only
+    ((300, 900, 1, 513, 256), 8, 2, 128, 256, None),    # the largest blocks: 16 tiles per block
 ]
 
 

@@ -47,6 +47,8 @@ CASES = [
     ((5, 600), 12, 3, 128, 128),
     ((40, 90), 8, 2, 64, 12),                       # not a power of two: CUDA-core kernel
     ((3000, 4000), 16, 4, 128, 16),                 # a wide split: merge kernel
+    ((5, 700), 8, 2, 128, 256),                     # the largest blocks
+    ((2, 33, 250), 8, 2, 64, 2),                    # blocks of 2: one bulk copy per token row
 ]
 
 

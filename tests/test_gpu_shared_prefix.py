@@ -46,6 +46,7 @@ CASES = [
     (1, (300,), 32, 8, 128, 128),                   # one sequence, one large block shared
     (9, (12, 250, 31), 24, 12, 128, 64),            # 12 KV heads
     (4, (1000, 2000, 5, 700), 32, 8, 128, 16),      # long rests: split, partitions merged by the merge kernel
+    (2, (10, 300, 0), 16, 4, 128, 256),             # the largest blocks: 512 shared tokens in two blocks
 ]
 
 

@@ -44,6 +44,8 @@ import workloads  # noqa: E402
 HBM_NOMINAL_GBS = 8000.0
 GRAPH_STEPS = 20          # steps captured per CUDA graph in the timed loop
 E2E_DEPTH = 3             # e2e steps in flight before the host reads a step's output
+E2E_MIN_STEPS = 2000      # e2e is timed over at least this many steps (the pipeline's fill and
+E2E_MAX_STEPS = 20000     #   drain would dominate a short run), and at most this many
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -83,6 +85,13 @@ def build_workload(config: str, rank: int, copies: int, block_size: int = 16, la
                              block_size=block_size), \
             "llama gqa: 64 seqs, len U[512,4096], Hq 32, Hkv 8, D 128, bf16, block %d" % block_size
     raise SystemExit(f"unknown config {config}")
+
+
+def workload_config(desc: str, kv_per_step: int) -> dict:
+    """``config`` of the JSON line: what the workload is, the same for both
+    arms (how each arm runs it goes elsewhere in the line)."""
+    return {"workload": desc,
+            "l2": "inputs larger than L2 (129 MB): each step reads %.0f MB of K/V" % (kv_per_step / 1e6)}
 
 
 def per_batch(config: str) -> int:
@@ -289,11 +298,14 @@ def run_reference(args, rank, world):
         seqs_done += len(seqs)
     value = kvb / total / 1e9
     line = {
-        "metric": "paged decode attention KV GB/s (Qwen3-8B shape)", "value": value, "unit": "GB/s",
-        "impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": ("paged decode attention KV GB/s (Qwen3-8B shape)" if args.config == "qwen3"
+                   else "paged decode attention KV GB/s (%s workload)" % args.config),
+        "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded)",
-        "config": {"workload": desc, "sample_seqs_per_step": per_step},
+        "config": workload_config(desc, kv_bytes(batch.context_lens, batch.num_kv_heads, batch.head_dim,
+                                                 batch.elem_bytes)),
+        "sample": {"seqs_per_step": per_step, "of": nb},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
                          "sample": f"{per_step} sequence(s) of the batch per step"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -306,6 +318,82 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------------------
 # the CUDA arm
 # ---------------------------------------------------------------------------
+def long_context_line(torch, pa, stream, reps: int, peak: float, peak_kind: str) -> dict:
+    """The long-context workload (4 x 32,768 tokens, Hq 64, Hkv 8, D 128, bf16,
+    blocks of 16) timed as the headline is: GRAPH_STEPS launches per CUDA
+    graph, two disjoint batches alternating, CUDA events on the launching
+    stream. The decode alone (pa_decode) gives the roofline fraction; the
+    whole step (pa_decode_append: the new tokens written, then the decode)
+    is timed the same way."""
+    copies = 2
+    batch, desc = build_workload("long", 0, copies)
+    nb = per_batch("long")
+    hq, hkv, d, bs = batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size
+
+    def dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    k_cache, v_cache = dev(batch.k_cache), dev(batch.v_cache)
+    views = []
+    for c in range(copies):
+        sl = slice(c * nb, (c + 1) * nb)
+        lens = batch.context_lens[sl]
+        views.append({"query": dev(batch.query[sl]), "tables": dev(batch.block_tables[sl]), "lens": dev(lens),
+                      "key": dev(batch.new_key[sl]), "value": dev(batch.new_value[sl]),
+                      "max_len": int(lens.max()), "lens_h": lens,
+                      "out": torch.empty((nb, hq, d), dtype=torch.float32, device="cuda")})
+    ws_bytes = max(pa.pa_decode_workspace_size(nb, hq, hkv, d, bs, v["max_len"]) for v in views)
+    workspace = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    plan = pa.pa_decode_plan(nb, hq, hkv, d, bs, max(v["max_len"] for v in views), with_workspace=True)
+
+    def decode(i):
+        v = views[i % copies]
+        pa.pa_decode(v["out"], v["query"], k_cache, v_cache, v["tables"], v["lens"], v["max_len"], batch.scale,
+                     workspace=workspace)
+
+    def step(i):
+        v = views[i % copies]
+        pa.pa_decode_append(v["out"], v["query"], v["key"], v["value"], k_cache, v_cache, v["tables"], v["lens"],
+                            v["max_len"], batch.scale, workspace=workspace)
+
+    def graph_of(fn):
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(GRAPH_STEPS):
+                fn(i)
+        return g
+
+    def per_launch_ms(g):
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * GRAPH_STEPS)
+
+    decode_ms = per_launch_ms(graph_of(decode))
+    step_ms = per_launch_ms(graph_of(step))
+    if pa.pa_device_status() != 0:
+        raise SystemExit("device status not clean after the long-context loops")
+    alg = np.mean([decode_alg_bytes(v["lens_h"], hq, hkv, d, bs, batch.elem_bytes) for v in views])
+    kvb = np.mean([kv_bytes(v["lens_h"], hkv, d, batch.elem_bytes) for v in views])
+    achieved = alg / (decode_ms * 1e-3) / 1e9
+    return {"workload": desc, "plan": plan, "decode_us": decode_ms * 1e3, "alg_bytes_per_launch": int(alg),
+            "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+            "pct_of_8tbs": 100.0 * achieved / HBM_NOMINAL_GBS,
+            "step_us": step_ms * 1e3, "step_kv_gbs": kvb / (step_ms * 1e-3) / 1e9,
+            "launches": reps * GRAPH_STEPS * 2}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -452,9 +540,6 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     ms_total = ev0.elapsed_time(ev1)
-    time.sleep(0.15)
-    sampler.stop()
-    clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
     steps_timed = K
 
     # the dominant kernel alone: decode-only graph replays, CUDA events on its stream
@@ -577,7 +662,7 @@ def run_ours(args, rank, world, local_rank):
         for sb in slots_e2e:
             read_back(sb)
 
-    e2e_steps = min(K, 2000)
+    e2e_steps = min(max(K, E2E_MIN_STEPS), E2E_MAX_STEPS)
     e2e_run(E2E_DEPTH + 1)
     torch.cuda.synchronize()
     if world > 1:
@@ -590,12 +675,29 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit("device status not clean after the timed region")
     if not np.isfinite(checksum[0]):
         raise SystemExit("non-finite decode output in the e2e loop")
+    peak, peak_kind = measured_peaks()
+    # the second workload the roofline target names: long contexts, decode timed the same way
+    long_ctx = (long_context_line(torch, pa, stream, dreps, peak, peak_kind)
+                if headline and args.config == "qwen3" else None)
+    t_end = time.perf_counter()
+    time.sleep(0.15)
+    sampler.stop()
+    # clocks over every timed loop of the run (the K steps, the decode-only
+    # loops and e2e); the K steps alone may be shorter than one sample
+    clocks = sampler.summary(t_wall0 - 0.05, t_end + 0.05)
+    clocks["timed_steps_samples"] = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)["samples"]
+    clocks["window"] = "timed steps, decode-only loops and e2e"
 
     # max over ranks
     ms_step = ms_total / steps_timed
     e2e_ms_step = e2e_s * 1e3 / e2e_steps
     if world > 1:
         ms_step, e2e_ms_step, decode_ms = max_over_ranks([ms_step, e2e_ms_step, decode_ms], "cuda")
+        if long_ctx is not None:
+            long_ctx["decode_us"], long_ctx["step_us"] = max_over_ranks(
+                [long_ctx["decode_us"], long_ctx["step_us"]], "cuda")
+            long_ctx["achieved"] = long_ctx["alg_bytes_per_launch"] / (long_ctx["decode_us"] * 1e-6) / 1e9
+            long_ctx["frac"] = long_ctx["achieved"] / peak
 
     lens0 = views[0]["lens_h"]
     step_kv = kv_bytes(lens0, hkv, d, elem)          # per batch; both batches have equal totals for qwen3/long
@@ -604,7 +706,6 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = whole_job_gbs(world, avg_kv, e2e_ms_step)
     alg = np.mean([decode_alg_bytes(v["lens_h"], hq, hkv, d, bs, elem) for v in views])
     achieved = alg / (decode_ms * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
     traffic = profiled_traffic(args.config, BALANCED_SOURCES if plan.get("balanced") else DECODE_SOURCES) \
         if headline else None
     if not plan["tensor_cores"]:
@@ -631,12 +732,13 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": ("synthetic (seeded N(0,1), bf16-rounded; one contiguous reservation per sequence)" if contig else
                  "synthetic (seeded N(0,1), bf16-rounded; block placement a seeded random permutation)"),
-        "config": {"workload": desc,
-                   "graphs": "%d steps per CUDA graph, %d batches alternate" % (GRAPH_STEPS, copies),
-                   "l2": "inputs larger than L2: 2 batches of %.0f MB alternate" % (step_kv / 1e6),
-                   "plan": plan,
-                   "step": ("reshape_and_cache(%d tokens) + pa_decode_contiguous" % nb if contig else
-                            "pa_decode_append: %d new tokens into their slots, then the decode" % nb)},
+        "config": workload_config(desc, step_kv),
+        "setup": {"graphs": "%d steps per CUDA graph" % GRAPH_STEPS,
+                  "batches": "%d disjoint batches of the workload alternate, so consecutive steps read "
+                             "disjoint memory" % copies,
+                  "plan": plan,
+                  "step": ("reshape_and_cache(%d tokens) + pa_decode_contiguous" % nb if contig else
+                           "pa_decode_append: %d new tokens into their slots, then the decode" % nb)},
         "tokens_per_s": world * nb / (ms_step * 1e-3),
         "pct_of_8tbs": 100.0 * value / HBM_NOMINAL_GBS,
         "pct_of_measured_hbm": 100.0 * value / peak,
@@ -653,6 +755,8 @@ def run_ours(args, rank, world, local_rank):
                        "reshape_and_cache_tokens": nb},
         "tokens_per_s_36_layers_attention_only": world * nb / (36 * ms_step * 1e-3),
     }
+    if long_ctx is not None:
+        line["long_context"] = long_ctx
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not contig:
         line["cpu_baseline"] = cpu_baseline(batch, nb, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -870,7 +974,7 @@ def run_cow(args, rank, world, local_rank):
 
     for i in range(3):
         e2e_step(i)
-    e2e_steps = min(K, 2000)
+    e2e_steps = min(max(K, E2E_MIN_STEPS), E2E_MAX_STEPS)
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         e2e_step(i)
@@ -1036,6 +1140,20 @@ def tables_bytes(lens, bs) -> int:
     return sum(workloads.cdiv(int(n), bs) for n in lens) * 4
 
 
+def spawn_ranks(nproc: int) -> int:
+    """``--gpus N`` run directly (not under a launcher): start this script on N
+    local ranks, one process per GPU, through torch.distributed.run with the
+    rendezvous on 127.0.0.1 and the same arguments; its exit status is the
+    launcher's. Each rank times its own batch (weak scaling); rank 0 prints."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=%d" % nproc,
+           "--master-addr=127.0.0.1", "--master-port=%d" % port, os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1058,6 +1176,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return spawn_ranks(args.gpus)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))

@@ -6,6 +6,9 @@
  * synchronise, and check their host arguments before any launch: a call that
  * returns anything but PA_OK has enqueued nothing. Faults inside a kernel
  * surface at the caller's next synchronisation, as usual in CUDA.
+ * State the library keeps (nothing else): one device status word per device
+ * (pa_device_status), the fixed scratch of pa_decode_static_scratch, and the
+ * second stream of pa_decode_shared_prefix (one per host thread and device).
  *
  * Conventions shared by every entry point
  *  - Pointers named *_cache, query, key, value, new_key, new_value, out,
@@ -104,7 +107,10 @@ PA_API pa_status pa_reshape_and_cache(const void *key, const void *value, void *
  *   block_mapping [num_pairs, 2] int64 (src, dst): block dst of k_cache and of
  *                 v_cache becomes a byte copy of block src.
  *   Preconditions: dst ids distinct and disjoint from src ids (otherwise
- *   the result depends on copy order). Pairs with an id outside
+ *   the result depends on copy order). They are not checked: the mapping is
+ *   device memory, and checking it would cost a copy to the host and a
+ *   synchronisation. pa_bm_append_slot only ever produces such pairs (each
+ *   dst is a block just taken from the free queue). Pairs with an id outside
  *   [0, num_blocks) are skipped. num_pairs == 0 is a no-op.
  * ---------------------------------------------------------------------- */
 PA_API pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_mapping,
@@ -255,6 +261,12 @@ PA_API pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *que
  *   Other arguments as pa_decode. Supported: bf16 or fp16 query and cache, head_dim
  *   64 or 128, block_size 8, 16, 32, 64, 128 or 256. With no whole tile
  *   shared this is pa_decode.
+ *   Streams: the prefix pass runs on a second stream of the library's own,
+ *   forked from `stream` and joined back into it by events, so the call stays
+ *   ordered on `stream` and can be captured into a CUDA graph. That stream is
+ *   created on the first call from each host thread on each device, and kept
+ *   until the process exits. PA_PREFIX_OVERLAP=0 runs both passes on `stream`
+ *   (no second stream is created).
  * ---------------------------------------------------------------------- */
 PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                                      int head_dim, int block_size,
@@ -309,18 +321,25 @@ PA_API pa_status pa_decode_contiguous(void *out, pa_dtype out_dtype, const void 
  * device memory is reserved up front by another allocator (cudaMalloc would
  * fail there or bypass its accounting), or a plugin interface that passes only
  * the operation's inputs and outputs. This entry point computes what pa_decode
- * computes, with the same arguments minus the workspace, and merges a context
- * split through a fixed scratch array built into the library:
- * PA_STATIC_SCRATCH_BYTES bytes of device memory that every GPU loading the
- * library holds until the process exits. It allocates nothing.
- *  - A problem whose split needs more scratch than that returns
+ * computes, with the same arguments minus the workspace, and allocates
+ * nothing. It splits a context as pa_decode given a workspace does (the
+ * ragged-balanced path aside): a split of up to 8 partitions is merged inside
+ * a thread-block cluster, in shared memory, and uses no scratch; a wider split
+ * writes its partial outputs, maxima and sums into a fixed scratch array built
+ * into the library, PA_STATIC_SCRATCH_BYTES bytes of device memory that every
+ * GPU loading the library holds until the process exits, and a merge kernel
+ * reads them back.
+ *  - A problem whose wider split needs more scratch than that returns
  *    PA_ERR_WORKSPACE before anything is launched (use pa_decode with a
  *    workspace of pa_decode_workspace_size() bytes instead).
+ *    pa_decode_plan(..., with_workspace = 1) reports the split and its
+ *    workspace_bytes for every shape it does not run ragged-balanced.
  *  - The first call on a device looks up the scratch's device address (with
  *    that device current); make that first call before any stream capture.
- *  - Every call shares the one scratch array and its arrival counters are
- *    cleared on `stream` at each call: calls that overlap on the GPU (other
- *    streams, other threads) race and give wrong results. Serialise them.
+ *  - Every call writes its partials into the one shared array (nothing in it
+ *    needs clearing: each call writes every entry it reads). Calls that
+ *    overlap on the GPU (other streams, other threads) therefore overwrite
+ *    each other's partials and give wrong results. Serialise them.
  * ---------------------------------------------------------------------- */
 #define PA_STATIC_SCRATCH_BYTES (8u << 20)
 PA_API pa_status pa_decode_static_scratch(void *out, pa_dtype out_dtype, const void *query,
@@ -372,6 +391,22 @@ PA_API pa_status pa_lse_merge(void *out, pa_dtype out_dtype, const float *tmp_ou
  * word to *status (after synchronising `stream`) and, if `clear`, resets it.
  * One word per device, shared by every call on that device. */
 PA_API pa_status pa_device_status(int *status, int clear, void *stream);
+
+/* Check of that failure detection on the current device. Launches, on
+ * `stream`, one CTA laid out as the decode kernels' pipeline (a producer warp
+ * arming a shared-memory stage, a consumer warp waiting for it) whose stage
+ * is armed for a copy that is never issued, so the consumer's bounded wait
+ * runs out after timeout_us microseconds instead of the kernels' 2 s. The
+ * CTA then records PA_ERR_TIMEOUT in the device status word, stops and
+ * returns, as a decode kernel would; no copy is ever in flight. Afterwards
+ * pa_device_status reports PA_ERR_TIMEOUT (and clears it if asked), and the
+ * device stays usable. The status word is shared: do not run this beside
+ * decode calls whose status you mean to read. (Not a step of the pages'
+ * method: it tests the library's own failure handling, the counterpart of
+ * which on the pages is preemption, "PagedAttention, explained.", procedure
+ * steps 7-8.)
+ *   timeout_us  1 .. 2,000,000 (else PA_ERR_INVALID_ARG). */
+PA_API pa_status pa_check_wait_timeout(unsigned timeout_us, void *stream);
 
 /* ------------------------------------------------------------------------
  * Host slot map: slot_mapping[i] = block_tables[seq[i]][pos[i] / block_size]

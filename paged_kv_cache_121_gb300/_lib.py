@@ -55,6 +55,7 @@ SIGNATURES = {
     "pa_lse_merge": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
                              c_int, c_int, c_int, c_int, c_void_p]),
     "pa_device_status": (c_int, [P_INT, c_int, c_void_p]),
+    "pa_check_wait_timeout": (c_int, [ctypes.c_uint, c_void_p]),
     "pa_compute_slot_mapping": (c_int, [P_I64, P_I32, c_int, c_int, P_I32, P_I32, c_int, c_int]),
     "pa_bm_create": (c_int, [c_int, c_int, c_int, ctypes.POINTER(c_void_p)]),
     "pa_bm_create_with_free_list": (c_int, [c_int, c_int, P_I32, c_int, ctypes.POINTER(c_void_p)]),

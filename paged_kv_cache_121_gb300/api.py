@@ -116,8 +116,11 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, max_cont
               workspace=None, stream=None) -> None:
     """Paged decode attention into ``out`` [B, Hq, D] (float32, bfloat16 or float16).
 
-    ``workspace`` is a zero-initialised uint8 tensor of at least
-    :func:`pa_decode_workspace_size` bytes, or None (no context split)."""
+    ``workspace`` is a uint8 tensor of at least :func:`pa_decode_workspace_size`
+    bytes (its contents need no initialisation; calls sharing it must not
+    overlap on the GPU), or None: then the tensor-core kernel merges a split of
+    up to 8 partitions inside a thread-block cluster and trims a wider one to
+    8, and the CUDA-core kernel does not split."""
     nb, bs, hkv, d = _cache_dims(k_cache)
     B, hq, dq = (int(x) for x in query.shape)
     ws_bytes = int(workspace.numel() * workspace.element_size()) if workspace is not None else 0
@@ -194,9 +197,10 @@ def pa_decode_contiguous(out, query, k, v, context_lens, max_context_len, scale,
 
 def pa_decode_static_scratch(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len,
                              scale, stream=None) -> None:
-    """pa_decode without a workspace argument: a context split is merged
-    through the library's own fixed scratch (for callers that cannot
-    allocate device memory; calls must not overlap on the GPU)."""
+    """pa_decode without a workspace argument, for callers that cannot
+    allocate device memory: a split of up to 8 partitions is merged inside a
+    thread-block cluster, a wider one through the library's own fixed
+    scratch (calls must not overlap on the GPU)."""
     nb, bs, hkv, d = _cache_dims(k_cache)
     B, hq, _ = (int(x) for x in query.shape)
     _check(_lib.load().pa_decode_static_scratch(
@@ -232,6 +236,13 @@ def pa_device_status(clear: bool = True, stream=None) -> int:
     v = ctypes.c_int(0)
     _check(_lib.load().pa_device_status(ctypes.byref(v), int(clear), _stream(stream)), "pa_device_status")
     return v.value
+
+
+def pa_check_wait_timeout(timeout_us: int = 1000, stream=None) -> None:
+    """Run the failure-detection check: one CTA's bounded wait on a stage no
+    copy fills runs out after ``timeout_us`` and records PA_ERR_TIMEOUT in the
+    device status word (read it with :func:`pa_device_status`)."""
+    _check(_lib.load().pa_check_wait_timeout(int(timeout_us), _stream(stream)), "pa_check_wait_timeout")
 
 
 def pa_compute_slot_mapping(block_tables: np.ndarray, seq_index, positions, block_size: int) -> np.ndarray:

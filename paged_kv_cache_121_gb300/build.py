@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libpa.so")
 
 SOURCES = ["api.cu", "decode_mma.cu", "decode_balanced.cu", "prefix_mma.cu", "prefix_tc.cu", "decode_simt.cu", "cache_ops.cu",
-           "decode_static.cu", "block_manager.cpp"]
+           "decode_static.cu", "health.cu", "block_manager.cpp"]
 HEADERS = ["device_common.cuh", "mma_tile.cuh", "tcgen05.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -623,6 +623,12 @@ pa_status check_prefix_call(const DecodeShape &s, pa_dtype q_dtype, pa_dtype kv_
 
 }  // namespace
 
+int *device_status_word() {
+    int dev;
+    if (current_device(&dev) != PA_OK) return nullptr;
+    return status_word(dev);
+}
+
 int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes, void *stream) {
     const DecodeShape s{c.num_seqs, c.num_heads, c.num_kv_heads, c.head_dim, c.block_size,
                         c.max_blocks_per_seq, c.num_blocks, c.max_context_len};
@@ -638,11 +644,13 @@ int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes
     if ((st = current_device(&dev)) != PA_OK) return st;
     const int sms = sm_count(dev);
     if (sms <= 0) return PA_ERR_CUDA;
-    Plan pl = plan_split(s, sms, use_mma(s, is16(kv_dtype)));
-    pl.cluster = false;   // the split, if any, goes through the scratch
+    // pa_decode's plan for a caller with a workspace, without the ragged-balanced
+    // path: a split that fits a thread-block cluster is merged there, in shared
+    // memory (no scratch); a wider one goes through the scratch.
+    const Plan pl = plan_split(s, sms, use_mma(s, is16(kv_dtype)));
+    const bool wide = !pl.cluster && pl.nsplit > 1;
     const WorkspaceLayout wl = workspace_layout(s, pl);
-    if (pl.nsplit > 1 && (wl.total > scratch_bytes || !scratch || !aligned16(scratch)))
-        return PA_ERR_WORKSPACE;
+    if (wide && (wl.total > scratch_bytes || !scratch || !aligned16(scratch))) return PA_ERR_WORKSPACE;
     if (!c.out || !c.query || !c.k_cache || !c.v_cache || !c.block_tables || !c.context_lens)
         return PA_ERR_INVALID_ARG;
     if (!aligned16(c.out) || !aligned16(c.query) || !aligned16(c.k_cache) || !aligned16(c.v_cache))
@@ -656,11 +664,11 @@ int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes
     p.heads_per_cta = pl.heads_per_cta;
     p.nsplit = pl.nsplit;
     p.part_tokens = pl.part_tokens;
-    p.cluster_merge = 0;
-    if (pl.nsplit > 1)
+    p.cluster_merge = pl.cluster ? 1 : 0;
+    if (wide)
         return launch_split_and_merge(s, p, kv_dtype, pl.mma, dev, scratch, wl, c.out, static_cast<int>(out_dtype),
                                       as_stream(stream));
-    p.mode = kModeFinal;
+    p.mode = kModeFinal;   // unsplit, or merged by the cluster
     return launch_decode(s, p, kv_dtype, pl.mma, dev, as_stream(stream));
 }
 

@@ -233,14 +233,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete; gives up after
-// kWaitLimitNs and returns false (the caller records a timeout and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// limit_ns and returns false (the caller records a timeout and unwinds).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 255u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// The kernels' wait: bounded by kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------------------

@@ -77,12 +77,20 @@ struct DecodeCall {
     float scale;
 };
 
-// Decode whose context split (when the plan splits) is always merged through
-// `scratch` (never inside a cluster). The arrival counters in the scratch are
-// cleared on `stream` before the launch. Returns a pa_status value;
-// PA_ERR_WORKSPACE (checked before any pointer) when the plan needs more
-// than scratch_bytes.
+// Decode with pa_decode's plan for a caller with a workspace, the
+// ragged-balanced path aside: a split that fits a thread-block cluster is
+// merged there; a wider one writes its partials into `scratch` and the merge
+// kernel reads them back (every entry it reads is written by the same call).
+// Returns a pa_status value; PA_ERR_WORKSPACE (checked before any pointer)
+// when a wider split needs more than scratch_bytes.
 int decode_into_scratch(const DecodeCall &c, void *scratch, size_t scratch_bytes, void *stream);
+
+// The device status word of the current device (nullptr on a CUDA error).
+int *device_status_word();
+// Launch the bounded-wait check (health.cu): one CTA waits on an mbarrier
+// phase that no copy completes, gives up after limit_ns and records a
+// timeout in `status`.
+cudaError_t launch_wait_timeout_check(int *status, unsigned long long limit_ns, cudaStream_t stream);
 
 cudaError_t launch_transfer_blocks(void *dst_k, void *dst_v, const void *src_k, const void *src_v,
                                    const int64_t *block_mapping, int num_pairs, int64_t src_blocks,

@@ -179,3 +179,9 @@ def test_block_manager_errors():
     assert bm.stats()["free_blocks"] == 2   # unchanged by the failed call
     with pytest.raises(pa.PAError):
         pa.BlockManager(4, 16, free_order=[1, 1])
+
+
+def test_wait_timeout_check_rejects_bad_limits_before_launch():
+    lib = _lib.load()
+    assert lib.pa_check_wait_timeout(0, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_check_wait_timeout(2000001, None) == pa.PA_ERR_INVALID_ARG

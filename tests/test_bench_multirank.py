@@ -56,3 +56,26 @@ def test_max_over_ranks_and_whole_job_value_gloo():
 def test_whole_job_value_single_rank():
     import bench
     assert bench.whole_job_gbs(1, 272891904.0, 0.0474) == pytest.approx(272891904.0 / 47.4e-6 / 1e9)
+
+
+def test_gpus_flag_starts_one_rank_per_gpu():
+    """``bench.py --gpus 2`` run directly starts two ranks itself (through
+    torch.distributed.run, rendezvous on 127.0.0.1) and rank 0 alone prints
+    one line for the whole job. The reference arm runs on the host, so this
+    needs no GPU: rank 0 times the oracle, rank 1 exits without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=root, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    line = lines[0]
+    assert line["n_gpus"] == 2 and line["impl"] == "reference" and line["steps"] == 1
+    assert line["value"] > 0 and line["config"]["workload"].startswith("qwen3-8b layer")

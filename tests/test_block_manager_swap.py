@@ -126,6 +126,57 @@ def test_swap_out_and_back_keeps_the_sharing_pattern():
     assert bm.swap_stats() == {"host_blocks": 8, "free_host_blocks": 8, "swapped_seqs": 0}
 
 
+# The beams-and-prompt case above worked out by hand from the rules on the
+# pages ("PagedAttention, explained.", procedure steps 7-8: a request's blocks
+# go out together; "Paged Attention: Virtual Memory for the KV Cache", "Inside
+# vLLM: the block pool": allocation pops the free queue's front, freed blocks
+# go back to its front). Pool of 16 with the null block reserved: queue 1..15.
+#   allocate(0, 12) -> [1, 2, 3]; forks share them; each beam's append takes
+#   the next block: beams 0/1/2 = [1,2,3,4] / [1,2,3,5] / [1,2,3,6].
+#   swap_out([0, 1, 2]): distinct blocks in order of first appearance
+#   1,2,3,4,5,6 -> CPU 0..5; beam 1 reads [0, 1, 2, 4].
+#   swap_in([2, 1, 0]): first appearance over beams 2, 1, 0 is CPU 0,1,2,5,4,3;
+#   GPU blocks 1..6 come back off the queue front in that order.
+HAND_SWAP_OUT = [(1, 0), (2, 1), (3, 2), (4, 3), (5, 4), (6, 5)]
+HAND_SWAP_IN = [(0, 1), (1, 2), (2, 3), (5, 4), (4, 5), (3, 6)]
+HAND_TABLES_AFTER = {0: [1, 2, 3, 6], 1: [1, 2, 3, 5], 2: [1, 2, 3, 4]}
+
+
+def _beams(mgr):
+    mgr.enable_swap(8)
+    mgr.allocate(0, 12)
+    mgr.fork(0, 1)
+    mgr.fork(0, 2)
+    for s in (0, 1, 2):
+        mgr.append_slot(s)
+
+
+def test_swap_model_matches_hand_worked_case():
+    """The oracle's block-manager model on the case worked out by hand."""
+    model = oracle.BlockManagerModel(16, 4)
+    _beams(model)
+    assert [model.block_table(s) for s in (0, 1, 2)] == [[1, 2, 3, 4], [1, 2, 3, 5], [1, 2, 3, 6]]
+    with pytest.raises(ValueError):
+        model.swap_out([0])                # shares the prompt with beams 1 and 2
+    assert model.swap_out([0, 1, 2]) == HAND_SWAP_OUT
+    assert model.block_table(1) == [0, 1, 2, 4]
+    assert model.stats()["free_blocks"] == 15 and model.free[:6] == [1, 2, 3, 4, 5, 6]
+    with pytest.raises(ValueError):
+        model.append_slot(1)
+    assert model.swap_in([2, 1, 0]) == HAND_SWAP_IN
+    assert {s: model.block_table(s) for s in (0, 1, 2)} == HAND_TABLES_AFTER
+    assert all(model.refcount[b] == 3 for b in (1, 2, 3))
+    assert model.host_free == [0, 1, 2, 5, 4, 3, 6, 7]
+
+
+def test_swap_libpa_matches_hand_worked_case():
+    bm = pa.BlockManager(16, 4)
+    _beams(bm)
+    assert bm.swap_out([0, 1, 2]).tolist() == [list(p) for p in HAND_SWAP_OUT]
+    assert bm.swap_in([2, 1, 0]).tolist() == [list(p) for p in HAND_SWAP_IN]
+    assert {s: bm.block_table(s) for s in (0, 1, 2)} == HAND_TABLES_AFTER
+
+
 def test_swap_is_all_or_nothing():
     bm = pa.BlockManager(10, 4)
     bm.enable_swap(2)

@@ -131,3 +131,80 @@ def test_append_refuses_before_launching():
     torch.cuda.synchronize()
     assert np.array_equal(bits(db.k_cache), before)
     assert np.array_equal(bits(ldb.k_cache), lbefore)
+
+
+# ---------------------------------------------------------------------------
+# The step bench.py times, at full size: the bench's own batches (two
+# disjoint batches of sequences in one pool), its workspace and plan, the
+# steps alternating between the two batches inside one CUDA graph. Caches bit
+# for bit and both batches' outputs against the oracle.
+# ---------------------------------------------------------------------------
+FULL = [
+    # bench config, plan the step must take (checked, so the test keeps
+    # covering the launch configuration the bench reports)
+    ("qwen3", dict(tensor_cores=1, cluster_merge=1, balanced=0, kernel_launches=1)),   # 8-CTA cluster merge
+    ("long", dict(tensor_cores=1, cluster_merge=0, balanced=0, kernel_launches=2)),    # workspace split + merge
+    ("gqa", dict(tensor_cores=1, balanced=1, kernel_launches=2)),                       # ragged-balanced
+]
+
+
+@pytest.mark.parametrize("config,plan_keys", FULL, ids=[c for c, _ in FULL])
+def test_append_full_size_bench_step(config, plan_keys):
+    import bench
+    import oracle
+    from gpu_cases import to_dev
+
+    batch, _ = bench.build_workload(config, 0, 2)
+    nb = bench.per_batch(config)
+    hq, hkv, d, bs = batch.num_heads, batch.num_kv_heads, batch.head_dim, batch.block_size
+    k_cache, v_cache = to_dev(batch.k_cache), to_dev(batch.v_cache)
+    views = []
+    for c in range(2):
+        sl = slice(c * nb, (c + 1) * nb)
+        lens = batch.context_lens[sl]
+        views.append(dict(sl=sl, query=to_dev(batch.query[sl]), tables=to_dev(batch.block_tables[sl]),
+                          lens=to_dev(lens), key=to_dev(batch.new_key[sl]), value=to_dev(batch.new_value[sl]),
+                          max_len=int(lens.max()),
+                          out=torch.full((nb, hq, d), float("nan"), dtype=torch.float32, device="cuda")))
+    for v in views:
+        plan = pa.pa_decode_plan(nb, hq, hkv, d, bs, v["max_len"], with_workspace=True)
+        assert {k: plan[k] for k in plan_keys} == plan_keys, plan
+    ws_bytes = max(pa.pa_decode_workspace_size(nb, hq, hkv, d, bs, v["max_len"]) for v in views)
+    # the bench leaves its workspace as the previous step left it; start from garbage here
+    ws = torch.randint(0, 256, (max(ws_bytes, 1),), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        v = views[i % 2]
+        pa.pa_decode_append(v["out"], v["query"], v["key"], v["value"], k_cache, v_cache, v["tables"],
+                            v["lens"], v["max_len"], batch.scale, workspace=ws)
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        step(0)
+        step(1)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for i in range(4):
+            step(i)
+    for v in views:
+        v["out"].fill_(float("nan"))
+    with torch.cuda.stream(stream):
+        g.replay()
+        g.replay()
+    torch.cuda.synchronize()
+    assert pa.pa_device_status(clear=True) == 0
+
+    # oracle: every sequence's new token at position len - 1, then fp64 attention per batch
+    k_want, v_want = batch.k_cache.copy(), batch.v_cache.copy()
+    seq = np.arange(batch.num_seqs)
+    slots = oracle.slot_mapping(batch.block_tables, seq, batch.context_lens - 1, bs)
+    oracle.reshape_and_cache(k_want, v_want, batch.new_key, batch.new_value, slots)
+    assert np.array_equal(to_host_bits(k_cache), k_want)
+    assert np.array_equal(to_host_bits(v_cache), v_want)
+    for v in views:
+        sl = v["sl"]
+        want = oracle.paged_attention(batch.query[sl], k_want, v_want, batch.block_tables[sl],
+                                      batch.context_lens[sl], batch.scale)
+        err = max_err(v["out"], want)
+        assert err <= ATOL, (config, err)

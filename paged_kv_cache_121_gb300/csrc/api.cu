@@ -146,6 +146,12 @@ int balance_mode() {
     return v;
 }
 
+//   PA_PREFIX_CTAS         CTAs the shared-prefix pass aims at (default: one per SM)
+int prefix_ctas_override() {
+    static const int v = env_int("PA_PREFIX_CTAS", 1, 65536);
+    return v;
+}
+
 int ring_override_kb() {
     static const int v = env_int("PA_DECODE_RING_KB", 16, 200);
     return v;
@@ -188,6 +194,50 @@ pa_status make_cache_map(CUtensorMap *map, const void *cache, int64_t num_blocks
     CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// Query [B, Hkv * G, D] (16-bit) as 5-D, innermost first: (dim within a 64-dim
+// half, half, head within the GQA group, KV head, sequence). A box of 64 dims
+// x 1 half x G heads x 1 KV head x seqs sequences is one row group's half of
+// Q: rows sequence * G + head, 128 bytes each, with the 128-byte swizzle (the
+// K-major operand layout of the tensor cores). Sequences past the batch read
+// as zeros.
+pa_status make_query_group_map(CUtensorMap *map, const void *query, int num_seqs, int num_kv_heads, int group,
+                               int head_dim, int seqs, bool f16) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return PA_ERR_CUDA;
+    const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 2;
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(head_dim / 64), static_cast<cuuint64_t>(group),
+                                static_cast<cuuint64_t>(num_kv_heads), static_cast<cuuint64_t>(num_seqs)};
+    const cuuint64_t strides[4] = {128, row, row * group, row * group * num_kv_heads};
+    const cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(group), 1, static_cast<cuuint32_t>(seqs)};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                     const_cast<void *>(query), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// Split-K partial outputs tmp_out [B, Hq, part_stride, D] fp32 as 4-D,
+// innermost first: (dim, partition, query head, sequence). A box of out_cols
+// dims x 1 partition x G heads x seqs sequences is 128-byte rows (sequence *
+// G + head) of one row group, with the 128-byte swizzle; the store clips
+// sequences past the batch.
+pa_status make_partials_store_map(CUtensorMap *map, void *tmp_out, int num_seqs, int num_heads, int part_stride,
+                                  int head_dim, int group, int seqs) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return PA_ERR_CUDA;
+    const cuuint64_t row = static_cast<cuuint64_t>(head_dim) * 4;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(part_stride),
+                                static_cast<cuuint64_t>(num_heads), static_cast<cuuint64_t>(num_seqs)};
+    const cuuint64_t strides[3] = {row, row * part_stride, row * part_stride * num_heads};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(prefix_tc_out_cols()), 1, static_cast<cuuint32_t>(group),
+                               static_cast<cuuint32_t>(seqs)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, tmp_out, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -559,12 +609,17 @@ struct PrefixPlan {
     int chunk_tokens;
     int chunks;          // prefix partitions (grid.x of the prefix pass)
     int row_groups;      // grid.z of the prefix pass
+    int seqs_per_group;  // tcgen05: whole sequences per row group of at most 128 rows
+    int tc_groups;       // tcgen05: row groups of the batch
+    int groups_per_cta;  // tcgen05: row groups one CTA serves (they share its K/V tiles)
     Plan suffix;         // the decode kernel's split of the rest (never a cluster)
     int part_stride;     // partitions per (sequence, head): chunks + suffix splits
 };
 
 PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms, bool tc) {
     PrefixPlan pp{};
+    // the tcgen05 pass takes row groups of whole sequences: at most 128 query heads per KV head
+    tc = tc && s.num_heads / s.num_kv_heads <= prefix_tc_max_rows();
     pp.tc = tc;
     // the prefix pass takes whole tiles; shared tokens past the last one go with the rest
     const int tile = tc ? prefix_tc_tile_tokens() : 16;
@@ -572,11 +627,18 @@ PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms, bool tc
     P = P / tile * tile;
     pp.prefix_tokens = static_cast<int>(P);
     const int group = s.num_heads / s.num_kv_heads;
-    const int rows = tc ? prefix_tc_rows_per_cta() : prefix_rows_per_cta();
-    pp.row_groups = static_cast<int>(cdiv64(static_cast<int64_t>(s.num_seqs) * group, rows));
+    if (tc) {
+        pp.seqs_per_group = prefix_tc_max_rows() / group;
+        pp.tc_groups = static_cast<int>(cdiv64(s.num_seqs, pp.seqs_per_group));
+        pp.groups_per_cta = pp.tc_groups >= 2 ? 2 : 1;
+        pp.row_groups = static_cast<int>(cdiv64(pp.tc_groups, pp.groups_per_cta));
+    } else {
+        pp.row_groups = static_cast<int>(cdiv64(static_cast<int64_t>(s.num_seqs) * group, prefix_rows_per_cta()));
+    }
     if (P > 0) {
         const int64_t per_chunk = static_cast<int64_t>(s.num_kv_heads) * pp.row_groups;
-        const int64_t cap = static_cast<int64_t>(sms) * (tc ? 1 : kCtasPerSmMma);
+        const int64_t cap = prefix_ctas_override() ? prefix_ctas_override()
+                                                   : static_cast<int64_t>(sms) * (tc ? 1 : kCtasPerSmMma);
         int64_t chunks = std::max<int64_t>(1, cap / per_chunk);
         chunks = std::min<int64_t>(chunks, std::max<int64_t>(1, P / std::max(kMinPrefixChunk, tile)));
         chunks = std::min<int64_t>(chunks, kMaxSplits);
@@ -950,16 +1012,22 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
         if (pp.tc) {
             // boxes of one block (up to a 64-token tile), one 64-dim half, one head
             const int box = std::min(block_size, prefix_tc_tile_tokens());
-            const int stage = prefix_tc_stage_bytes(head_dim);
-            pq.ring_bytes = std::max(stage, std::min(kTcMaxRingBytes, ring_kb() * 1024) / stage * stage);
+            pq.ring_bytes = prefix_tc_ring_bytes(head_dim, pp.groups_per_cta, ring_kb() * 1024);
+            pq.seqs_per_group = pp.seqs_per_group;
+            pq.row_groups = pp.tc_groups;
+            CUtensorMap tq, to;
             if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1,
                                      pq.kv_f16 != 0)) != PA_OK ||
                 (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1,
-                                     pq.kv_f16 != 0)) != PA_OK) {
+                                     pq.kv_f16 != 0)) != PA_OK ||
+                (st = make_query_group_map(&tq, query, num_seqs, num_kv_heads, pq.group, head_dim,
+                                           pp.seqs_per_group, pq.kv_f16 != 0)) != PA_OK ||
+                (st = make_partials_store_map(&to, tmp_out, num_seqs, num_heads, pp.part_stride, head_dim, pq.group,
+                                              pp.seqs_per_group)) != PA_OK) {
                 join();
                 return st;
             }
-            if (launch_prefix_tc(pq, tk, tv, grid, pstrm) != cudaSuccess) {
+            if (launch_prefix_tc(pq, pp.groups_per_cta, tk, tv, tq, to, grid, pstrm) != cudaSuccess) {
                 join();
                 return PA_ERR_CUDA;
             }

@@ -125,6 +125,8 @@ struct PrefixParams {
     int part_stride;              // partitions per row in tmp_out
     int ring_bytes;
     int kv_f16;                   // query and caches are fp16 (else bf16)
+    int seqs_per_group;           // tcgen05 pass: whole sequences per row group (rows = this x group)
+    int row_groups;               // tcgen05 pass: row groups of the batch
     float scale_log2;
 };
 

@@ -26,13 +26,20 @@ int prefix_rows_per_cta();
 int prefix_stage_bytes(int head_dim);
 cudaError_t launch_prefix_mma(const PrefixParams &p, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                               dim3 grid, cudaStream_t stream);
-// Shared-prefix pass on tcgen05 (prefix_tc.cu): grid (chunks, Hkv, row groups of 128).
+// Shared-prefix pass on tcgen05 (prefix_tc.cu): grid (chunks, Hkv, cdiv(row groups, groups_per_cta)).
+// A row group is floor(128 / G) whole sequences x their G query heads (G <= 128).
 constexpr int kTcMaxRingBytes = 128 * 1024;
 constexpr int kTcChunkBlocks = 256;   // most block ids one chunk of the tcgen05 pass may span
-int prefix_tc_rows_per_cta();
+int prefix_tc_max_rows();             // rows of a row group at most (tensor-memory lanes)
 int prefix_tc_tile_tokens();
 int prefix_tc_stage_bytes(int head_dim);
-cudaError_t launch_prefix_tc(const PrefixParams &p, const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+int prefix_tc_out_cols();             // fp32 columns per box of the partial-output store map
+// ring bytes for a budget, clamped to what the kernel needs and its shared memory allows
+int prefix_tc_ring_bytes(int head_dim, int groups_per_cta, int budget_bytes);
+// tmap_q: query as (dim, half, head in group, KV head, sequence), box (64, 1, G, 1, seqs_per_group);
+// tmap_o: tmp_out as (dim, partition, head, sequence), box (out_cols, 1, G, seqs_per_group), fp32
+cudaError_t launch_prefix_tc(const PrefixParams &p, int groups_per_cta, const CUtensorMap &tmap_k,
+                             const CUtensorMap &tmap_v, const CUtensorMap &tmap_q, const CUtensorMap &tmap_o,
                              dim3 grid, cudaStream_t stream);
 // Balanced decode (decode_balanced.cu): the batch's tiles, concatenated
 // sequence after sequence, cut into `ctas` equal ranges per (KV-head group,

@@ -47,6 +47,8 @@ CASES = [
     (9, (12, 250, 31), 24, 12, 128, 64),            # 12 KV heads
     (4, (1000, 2000, 5, 700), 32, 8, 128, 16),      # long rests: split, partitions merged by the merge kernel
     (2, (10, 300, 0), 16, 4, 128, 256),             # the largest blocks: 512 shared tokens in two blocks
+    (3, tuple(range(5, 75)), 12, 2, 128, 16),       # G = 6: row groups of 21 sequences (126 rows), two pairs
+    (2, tuple(range(0, 70)), 32, 8, 64, 32),        # three row groups: the second pair holds one
 ]
 
 

@@ -428,7 +428,7 @@ pa_status launch_split_and_merge(const DecodeShape &s, DecodeParams &p, pa_dtype
     if (st != PA_OK) return st;
     const cudaError_t e = launch_lse_merge(out, out_type, p.tmp_out, p.max_logits, p.exp_sums,
                                            p.context_lens, s.num_seqs, s.num_heads, s.head_dim,
-                                           p.nsplit, p.part_tokens, stream);
+                                           p.nsplit, p.part_tokens, sm_count(dev), stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -1068,7 +1068,8 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     if (st != PA_OK) return st;
     // 3. merge all partitions of every row
     const cudaError_t e = launch_lse_merge(out, static_cast<int>(out_dtype), tmp_out, max_logits, exp_sums,
-                                           context_lens, num_seqs, num_heads, head_dim, pp.part_stride, 0, strm);
+                                           context_lens, num_seqs, num_heads, head_dim, pp.part_stride, 0, sms,
+                                           strm);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -1141,9 +1142,14 @@ PA_API pa_status pa_lse_merge(void *out, pa_dtype out_dtype, const float *tmp_ou
     if (num_seqs > 65535 || static_cast<size_t>(max_partitions) * sizeof(float) > 200 * 1024)
         return PA_ERR_UNSUPPORTED;
     if (!out || !tmp_out || !max_logits || !exp_sums || !context_lens) return PA_ERR_INVALID_ARG;
+    int dev;
+    pa_status st = current_device(&dev);
+    if (st != PA_OK) return st;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return PA_ERR_CUDA;
     cudaError_t e = launch_lse_merge(out, static_cast<int>(out_dtype), tmp_out, max_logits, exp_sums,
                                      context_lens, num_seqs, num_heads, head_dim, max_partitions,
-                                     partition_size, as_stream(stream));
+                                     partition_size, sms, as_stream(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -193,8 +193,28 @@ cudaError_t launch_decode_simt(const DecodeParams &p, int kv_type, dim3 grid, cu
     return cudaErrorInvalidValue;
 }
 
+__device__ __forceinline__ void store_merged(void *out, int out_type, int64_t idx, float v) {
+    if (out_type == 1)
+        reinterpret_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+    else if (out_type == 2)
+        reinterpret_cast<__half *>(out)[idx] = __float2half_rn(v);
+    else
+        reinterpret_cast<float *>(out)[idx] = v;
+}
+
 // ---------------------------------------------------------------------------
-// log-sum-exp merge of split-K partitions: one CTA per (head, sequence)
+// log-sum-exp merge of split-K partitions: one CTA per (head, sequence).
+// Two forms of the same merge (an empty partition has sum 0 and weight 0):
+//  * lse_merge_kernel, for many rows (CTAs) per SM: warp 0 turns every
+//    partition's max and sum into a weight in shared memory, once per CTA,
+//    then every thread combines its output dim's values; few registers, so
+//    many CTAs stay resident and hide each other's latency.
+//  * lse_merge_online_kernel, for few rows per SM (long contexts: a handful
+//    of CTAs, each latency-bound): no barrier. Partitions are taken eight at a
+//    time: every lane issues its column's eight values while lane j < 8 loads
+//    partition j's max and sum, so a batch costs one round trip to L2; the
+//    warp moves its running max by a shuffle reduction, lane j computes
+//    partition j's weight, and the weights are broadcast by shuffles.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128)
 lse_merge_kernel(void *out, int out_type, const float *tmp_out, const float *max_logits,
@@ -237,28 +257,81 @@ lse_merge_kernel(void *out, int out_type, const float *tmp_out, const float *max
         const float *src = tmp_out + row0 * head_dim + d;
 #pragma unroll 8
         for (int q = 0; q < np; ++q) acc += wgt[q] * __ldcg(src + static_cast<int64_t>(q) * head_dim);
-        const int64_t oi = (static_cast<int64_t>(b) * num_heads + h) * head_dim + d;
-        if (out_type == 1)
-            reinterpret_cast<__nv_bfloat16 *>(out)[oi] = __float2bfloat16_rn(acc * inv);
-        else if (out_type == 2)
-            reinterpret_cast<__half *>(out)[oi] = __float2half_rn(acc * inv);
-        else
-            reinterpret_cast<float *>(out)[oi] = acc * inv;
+        store_merged(out, out_type, (static_cast<int64_t>(b) * num_heads + h) * head_dim + d, acc * inv);
+    }
+}
+
+constexpr int kMergeBatch = 8;
+
+__global__ void __launch_bounds__(128)
+lse_merge_online_kernel(void *out, int out_type, const float *tmp_out, const float *max_logits,
+                        const float *exp_sums, const int32_t *context_lens, int num_heads, int head_dim,
+                        int max_partitions, int partition_size) {
+    const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x & 31;
+    grid_dependency_wait();
+    grid_dependents_launch();
+    int len = context_lens[b];
+    if (len < 0) len = 0;
+    const int np = partition_size > 0 ? min((len + partition_size - 1) / partition_size, max_partitions)
+                                      : max_partitions;
+    const int64_t row0 = (static_cast<int64_t>(b) * num_heads + h) * max_partitions;
+    const float *ml = max_logits + row0, *es = exp_sums + row0;
+    // (warp-uniform trip counts: every lane of a warp takes part in the shuffles)
+    for (int d0 = threadIdx.x & ~31; d0 < head_dim; d0 += blockDim.x) {
+        const int d = d0 + lane;
+        const bool col = d < head_dim;
+        const float *src = tmp_out + row0 * head_dim + d;
+        float M = -INFINITY, L = 0.f, acc = 0.f;
+        for (int q0 = 0; q0 < np; q0 += kMergeBatch) {
+            float o[kMergeBatch];
+#pragma unroll
+            for (int j = 0; j < kMergeBatch; ++j)
+                o[j] = (col && q0 + j < np) ? __ldcg(src + static_cast<int64_t>(q0 + j) * head_dim) : 0.f;
+            const bool mine = lane < kMergeBatch && q0 + lane < np;   // lane j: partition q0 + j
+            const float lj = mine ? __ldcg(es + q0 + lane) : 0.f;
+            const float mj = mine ? __ldcg(ml + q0 + lane) : -INFINITY;
+            float Mc = lj > 0.f ? mj : -INFINITY;
+#pragma unroll
+            for (int off = kMergeBatch / 2; off; off >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, off));
+            Mc = fmaxf(__shfl_sync(0xffffffffu, Mc, 0), M);
+            if (Mc > M) {   // the running max moves: rescale what is summed so far
+                const float sc = fast_exp2((M - Mc) * kLog2e);
+                L *= sc;
+                acc *= sc;
+                M = Mc;
+            }
+            const float wj = lj > 0.f ? lj * fast_exp2((mj - M) * kLog2e) : 0.f;
+#pragma unroll
+            for (int j = 0; j < kMergeBatch; ++j) {
+                const float w = __shfl_sync(0xffffffffu, wj, j);
+                L += w;
+                acc += w * o[j];
+            }
+        }
+        if (col) store_merged(out, out_type, (static_cast<int64_t>(b) * num_heads + h) * head_dim + d,
+                              L > 0.f ? acc / L : 0.f);
     }
 }
 
 cudaError_t launch_lse_merge(void *out, int out_type, const float *tmp_out, const float *max_logits,
                              const float *exp_sums, const int32_t *context_lens, int num_seqs,
                              int num_heads, int head_dim, int max_partitions, int partition_size,
-                             cudaStream_t stream) {
+                             int sms, cudaStream_t stream) {
+    if (head_dim <= 0) return cudaErrorInvalidValue;
+    const unsigned threads = head_dim >= 128 ? 128u : static_cast<unsigned>((head_dim + 31) / 32 * 32);
+    dim3 grid(num_heads, num_seqs);
+    const int64_t rows = static_cast<int64_t>(num_seqs) * num_heads;
+    if (rows <= static_cast<int64_t>(kMergeOnlineRowsPerSm) * sms)
+        return launch_kernel(lse_merge_online_kernel, grid, dim3(threads), 0, stream, 1u, out, out_type, tmp_out,
+                             max_logits, exp_sums, context_lens, num_heads, head_dim, max_partitions,
+                             partition_size);
     const size_t smem = sizeof(float) * static_cast<size_t>(max_partitions);
     if (smem > 48 * 1024) {
         static unsigned long long done = 0;
         cudaError_t e = ensure_smem_limit(lse_merge_kernel, 200 * 1024, done);
         if (e != cudaSuccess) return e;
     }
-    dim3 grid(num_heads, num_seqs);
-    return launch_kernel(lse_merge_kernel, grid, dim3(128), smem, stream, 1u, out, out_type, tmp_out,
+    return launch_kernel(lse_merge_kernel, grid, dim3(threads), smem, stream, 1u, out, out_type, tmp_out,
                          max_logits, exp_sums, context_lens, num_heads, head_dim, max_partitions,
                          partition_size);
 }

@@ -61,10 +61,14 @@ cudaError_t launch_append_last(const void *key, const void *value, void *k_cache
                                cudaStream_t stream);
 // kv_type / out_type: 0 fp32, 1 bf16, 2 fp16 (the public dtype codes)
 cudaError_t launch_decode_simt(const DecodeParams &p, int kv_type, dim3 grid, cudaStream_t stream);
+// The log-sum-exp merge; `sms` (the device's SM count) picks its form: with
+// at most kMergeOnlineRowsPerSm (sequence, head) rows per SM, the
+// barrier-free online merge (latency-bound), else the shared-weights one.
+constexpr int kMergeOnlineRowsPerSm = 4;
 cudaError_t launch_lse_merge(void *out, int out_type, const float *tmp_out, const float *max_logits,
                              const float *exp_sums, const int32_t *context_lens, int num_seqs,
                              int num_heads, int head_dim, int max_partitions, int partition_size,
-                             cudaStream_t stream);
+                             int sms, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void *key, const void *value, void *k_cache,
                                      void *v_cache, const int64_t *slot_mapping, int num_tokens,
                                      int64_t num_slots, int row_bytes, cudaStream_t stream);

@@ -170,6 +170,33 @@ def test_splitk_partitions_and_merge(bs, ps):
     assert_clean_status()
 
 
+@pytest.mark.parametrize("num_seqs,hq", [(2, 8), (48, 32)])
+def test_lse_merge_few_and_many_rows(num_seqs, hq):
+    """pa_lse_merge takes one of two forms by (sequence, head) rows per SM: a
+    barrier-free online merge for few rows, shared-memory weights for many.
+    Both must give whole-context attention: ragged lengths leave trailing
+    partitions empty, and 19 partitions span several batches of eight."""
+    rng = np.random.default_rng(num_seqs)
+    lens = rng.integers(1, 19 * 64 + 1, size=num_seqs).astype(np.int32)
+    lens[0] = 19 * 64
+    hkv, d, bs, ps = hq // 4, 128, 16, 64
+    need = sum(workloads.cdiv(int(n), bs) for n in lens)
+    batch = workloads.make_batch("merge", lens, hq, hkv, d, bs, need + 3, True, seed_values=70 + num_seqs)
+    db = DeviceBatch(batch)
+    P = workloads.cdiv(int(lens.max()), ps)
+    tmp = torch.full((num_seqs, hq, P, d), float("nan"), dtype=torch.float32, device="cuda")
+    ml = torch.full((num_seqs, hq, P), float("nan"), dtype=torch.float32, device="cuda")
+    es = torch.full((num_seqs, hq, P), float("nan"), dtype=torch.float32, device="cuda")
+    pa.pa_decode_splitk(tmp, ml, es, ps, db.query, db.k_cache, db.v_cache, db.block_tables,
+                        db.context_lens, int(lens.max()), batch.scale)
+    out = torch.empty((num_seqs, hq, d), dtype=torch.float32, device="cuda")
+    pa.pa_lse_merge(out, tmp, ml, es, db.context_lens, ps)
+    want = oracle.paged_attention(batch.query, batch.k_cache, batch.v_cache, batch.block_tables,
+                                  batch.context_lens, batch.scale)
+    assert max_err(out, want) <= ATOL
+    assert_clean_status()
+
+
 # ---------------------------------------------------------------------------
 # scatter and copy: bit-exact
 # ---------------------------------------------------------------------------

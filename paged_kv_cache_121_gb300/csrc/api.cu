@@ -24,8 +24,9 @@ __device__ int g_device_status;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kCtasPerSmMma = 2;      // resident CTAs per SM the split plan aims at
-constexpr int kCtasPerSmSimt = 2;     //   (tensor-core / CUDA-core kernel)
+constexpr int kCtasPerSmMma = 2;      // CTAs per SM the split plan aims at: tensor-core kernel,
+constexpr int kCtasPerSmSimt = 12;    //   CUDA-core kernel (its 4-warp CTAs are latency-bound: more of
+                                      //   them hide more; Qwen3 layer 558 -> 238 us from 2 to 12)
 constexpr int kMmaHeadsPerCta = 4;    // KV heads per tensor-core CTA (consumer warps)
 constexpr int kContiguousTile = 16;   // tokens per tile of a contiguous cache
 constexpr int kMmaRingKiB = 96;       // shared-memory ring per tensor-core CTA: three stages when a

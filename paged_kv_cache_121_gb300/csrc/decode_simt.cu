@@ -3,10 +3,11 @@
 // log-sum-exp merge of split-K partitions.
 //
 // Same work decomposition and epilogue as the tensor-core kernel: one CTA per
-// (sequence, KV head, head tile, partition). Each warp takes every fourth
-// token of the partition; a lane owns head_dim/32 consecutive dims (one
-// coalesced vector load per K or V row), dot products are reduced with warp
-// shuffles, and the online softmax runs in fp32 in base 2.
+// (sequence, KV head, head tile, partition). The four warps take the
+// partition's tokens four at a time, round robin; a lane owns head_dim/32
+// consecutive dims (one coalesced vector load per K or V row), a warp loads
+// its four tokens' K and V rows before using any, dot products are reduced
+// with warp shuffles, and the online softmax runs in fp32 in base 2.
 // Pages: "What Does PagedAttention Actually Optimize?", sections 8, 14 and
 // 17 (read_kv: logical block = t / B, offset = t % B, physical block from the
 // table).
@@ -109,32 +110,62 @@ decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     const int32_t *table = p.block_tables + static_cast<int64_t>(b) * p.max_blocks;
     const int t_begin = w.tok_begin;
     const int t_end = w.tok_end;
-    for (int t = t_begin + warp; t < t_end; t += kWarps) {
-        const int64_t phys = table[t / p.block_size];
-        float kx[E], vx[E];
-        if (phys >= 0 && phys < p.num_blocks) {
-            const int64_t row = ((phys * p.block_size + t % p.block_size) * p.num_kv_heads + g) * D + lane * E;
-            RowLoad<E, KV>::load(kc + row, kx);
-            RowLoad<E, KV>::load(vc + row, vx);
-        } else {
+    // Each warp takes kTok consecutive tokens per iteration and loads all
+    // their K and V rows before using any (2 kTok row loads in flight per
+    // warp), then folds the kTok scores of each query row into its online
+    // softmax at once. A block id outside the pool reads as zeros.
+    constexpr int kTok = 4;
+    for (int t0 = t_begin + warp * kTok; t0 < t_end; t0 += kWarps * kTok) {
+        float kx[kTok][E], vx[kTok][E];
 #pragma unroll
-            for (int e = 0; e < E; ++e) kx[e] = vx[e] = 0.f;
+        for (int u = 0; u < kTok; ++u) {
+            const int t = t0 + u;
+            const int64_t phys = t < t_end ? table[t / p.block_size] : -1;
+            if (phys >= 0 && phys < p.num_blocks) {
+                const int64_t row = ((phys * p.block_size + t % p.block_size) * p.num_kv_heads + g) * D + lane * E;
+                RowLoad<E, KV>::load(kc + row, kx[u]);
+                RowLoad<E, KV>::load(vc + row, vx[u]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) kx[u][e] = vx[u][e] = 0.f;
+            }
         }
 #pragma unroll
         for (int r = 0; r < MAXR; ++r) {
             if (r >= rows) break;
-            float s = 0.f;
+            float s[kTok];
 #pragma unroll
-            for (int e = 0; e < E; ++e) s = fmaf(q[r][e], kx[e], s);
+            for (int u = 0; u < kTok; ++u) {
+                float acc = 0.f;
 #pragma unroll
-            for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-            s *= p.scale_log2;
-            const float mn = fmaxf(m[r], s);
+                for (int e = 0; e < E; ++e) acc = fmaf(q[r][e], kx[u][e], acc);
+                s[u] = acc;
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1)
+#pragma unroll
+                for (int u = 0; u < kTok; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+            float mn = m[r];
+#pragma unroll
+            for (int u = 0; u < kTok; ++u) {
+                s[u] = t0 + u < t_end ? s[u] * p.scale_log2 : -INFINITY;   // tokens past the partition: weight 0
+                mn = fmaxf(mn, s[u]);
+            }
             const float a = fast_exp2(m[r] - mn);
-            const float pr = fast_exp2(s - mn);
-            l[r] = l[r] * a + pr;
+            float pr[kTok], ps = 0.f;
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[r][e] = fmaf(o[r][e], a, pr * vx[e]);
+            for (int u = 0; u < kTok; ++u) {
+                pr[u] = fast_exp2(s[u] - mn);
+                ps += pr[u];
+            }
+            l[r] = l[r] * a + ps;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                float acc = o[r][e] * a;
+#pragma unroll
+                for (int u = 0; u < kTok; ++u) acc = fmaf(pr[u], vx[u][e], acc);
+                o[r][e] = acc;
+            }
             m[r] = mn;
         }
     }

@@ -14,9 +14,10 @@ decode step must read (valid tokens only) divided by the device time per step,
 with inputs resident in HBM. Two batches alternate so that consecutive steps
 read disjoint 273 MB sets (L2 is 129 MB). ``e2e`` is the wall-clock rate of
 the same steps with every step's inputs copied from pinned host memory and
-its output copied back and read on the host; copies run on their own stream
-beside the kernels (captured from the public calls into CUDA graphs), a few
-steps in flight.
+its output copied back and read on the host: each step is one CUDA graph
+captured from the public call, the upload of the next step's inputs and the
+download of the previous step's output on a second stream beside its kernels;
+the host reads each output two steps later.
 
 ``--impl reference`` times the oracle (fp64 CPU) on the host cores instead,
 one bounded sample of the workload per step.
@@ -529,6 +530,11 @@ def run_ours(args, rank, world, local_rank):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
+        # one more untimed graph of steps first, not waited for: the GPU is busy
+        # with it while the timed graphs are submitted, so the start event is
+        # followed at once by the K timed steps (no graph-launch latency inside
+        # the window); the batches keep alternating across the boundary
+        multi_step.replay()
         ev0.record(stream)
         for _ in range(K // GRAPH_STEPS):
             multi_step.replay()
@@ -556,16 +562,17 @@ def run_ours(args, rank, world, local_rank):
     scatter_ms, _ = time_graph(torch, stream, lambda i: scatter(views[i % copies]), dreps)
 
     # e2e through the public API, host buffers (pinned), copies inside the timed
-    # region. Every step copies its inputs (query, new K/V, tables, lengths,
-    # slots: one packed pinned buffer, one transfer) to the device, runs the
-    # scatter and the decode (captured once from the public calls into a CUDA
-    # graph per buffer set, as a serving engine captures its decode step),
-    # and copies the output back to pinned host memory, where the host reads
-    # it. Steps are pipelined E2E_DEPTH deep over two streams ordered by
-    # events: the kernels on one, the copies on the other, where step i + 1's
-    # upload is queued before step i's download, so that both overlap the
-    # kernels. The host reads a step's output when it comes back to that
-    # step's buffers.
+    # region. Every step copies its inputs (query, new K/V, lengths, slots,
+    # tables: one packed pinned buffer, one transfer) to the device, runs the
+    # step's public call (pa_decode_append; for the contiguous layout the
+    # scatter and pa_decode_contiguous), and copies the output back to pinned
+    # host memory, where the host reads it. Each step is one CUDA graph
+    # captured from those calls, as a serving engine captures its decode
+    # step: on the step's stream the kernels of step i, and beside them, on a
+    # second stream forked and joined inside the graph, the upload of step
+    # i + 1's inputs and the download of step i - 1's output. E2E_DEPTH buffer
+    # sets rotate; the host replays step i's graph, then waits for step i - 1's
+    # graph and reads step i - 2's output (which that graph downloaded).
     def pack(arrays):
         offs, pos = [], 0
         for a in arrays:
@@ -599,76 +606,73 @@ def run_ours(args, rank, world, local_rank):
             n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
             return stage[o:o + n].view(dtype).view(shape)
 
-        sb = {"stage": stage, "q": view(0, kv_t, arr0[0].shape), "k": view(1, kv_t, arr0[1].shape),
-              "v": view(2, kv_t, arr0[2].shape), "lens": view(3, torch.int32, arr0[3].shape),
-              "slots": view(4, torch.int64, arr0[4].shape),
-              "tables": None if contig else view(5, torch.int32, arr0[5].shape),
-              "out": torch.empty((nb, hq, d), dtype=torch.float32, device="cuda"),
-              "h_out": torch.empty((nb, hq, d), dtype=torch.float32).pin_memory(),
-              "up": torch.cuda.Event(), "run": torch.cuda.Event(), "down": torch.cuda.Event(),
-              "pending": False, "graphs": []}
-        for c in range(copies):
-            with torch.cuda.stream(s_e2e):
-                sb["stage"].copy_(staged[c][0])
-                for _ in range(2):   # warm up outside the capture
-                    pa.pa_reshape_and_cache(sb["k"], sb["v"], k_cache, v_cache, sb["slots"])
-                    decode_into(sb["out"], views[c], sb["q"], sb["lens"], sb["tables"])
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s_e2e, capture_error_mode="thread_local"):
-                if contig:
-                    pa.pa_reshape_and_cache(sb["k"], sb["v"], k_cache, v_cache, sb["slots"])
-                    decode_into(sb["out"], views[c], sb["q"], sb["lens"], sb["tables"])
-                else:
-                    pa.pa_decode_append(sb["out"], sb["q"], sb["k"], sb["v"], k_cache, v_cache, sb["tables"],
-                                        sb["lens"], views[c]["max_len"], batch.scale, workspace=workspace)
-            sb["graphs"].append(g)
-        return sb
+        return {"stage": stage, "q": view(0, kv_t, arr0[0].shape), "k": view(1, kv_t, arr0[1].shape),
+                "v": view(2, kv_t, arr0[2].shape), "lens": view(3, torch.int32, arr0[3].shape),
+                "slots": view(4, torch.int64, arr0[4].shape),
+                "tables": None if contig else view(5, torch.int32, arr0[5].shape),
+                "out": torch.empty((nb, hq, d), dtype=torch.float32, device="cuda"),
+                "h_out": torch.empty((nb, hq, d), dtype=torch.float32).pin_memory(),
+                "done": torch.cuda.Event()}
 
     slots_e2e = [slot_buffers() for _ in range(E2E_DEPTH)]
     d2h = slots_e2e[0]["h_out"].numel() * 4
+    period = E2E_DEPTH * copies // math.gcd(E2E_DEPTH, copies)   # graphs differ by (slot, batch)
+
+    def step_kernels(sb, c):
+        if contig:
+            pa.pa_reshape_and_cache(sb["k"], sb["v"], k_cache, v_cache, sb["slots"])
+            decode_into(sb["out"], views[c], sb["q"], sb["lens"], sb["tables"])
+        else:
+            pa.pa_decode_append(sb["out"], sb["q"], sb["k"], sb["v"], k_cache, v_cache, sb["tables"],
+                                sb["lens"], views[c]["max_len"], batch.scale, workspace=workspace)
+
+    def e2e_body(i):   # captured: step i's kernels, beside them step i + 1's upload and step i - 1's download
+        cur, nxt, prv = (slots_e2e[(i + x) % E2E_DEPTH] for x in (0, 1, E2E_DEPTH - 1))
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        fork.record(s_e2e)
+        s_copy.wait_event(fork)
+        with torch.cuda.stream(s_copy):
+            nxt["stage"].copy_(staged[(i + 1) % copies][0], non_blocking=True)
+            prv["h_out"].copy_(prv["out"], non_blocking=True)
+            join.record(s_copy)
+        step_kernels(cur, i % copies)
+        s_e2e.wait_event(join)
+
+    # warm-up outside any capture, then one graph per (slot, batch) pattern
+    with torch.cuda.stream(s_e2e):
+        for c in range(copies):
+            slots_e2e[c % E2E_DEPTH]["stage"].copy_(staged[c][0])
+        for i in range(period):
+            e2e_body(i)
+    torch.cuda.synchronize()
+    e2e_graphs = []
+    for i in range(period):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s_e2e, capture_error_mode="thread_local"):
+            e2e_body(i)
+        e2e_graphs.append(g)
     checksum = [0.0]
 
-    def read_back(sb):
-        if sb["pending"]:
-            sb["down"].synchronize()
-            checksum[0] += float(sb["h_out"][0, 0, 0])   # the step's result, read on the host
-            sb["pending"] = False
-
-    def upload(i):   # on s_copy
-        sb = slots_e2e[i % E2E_DEPTH]
-        read_back(sb)   # the buffers' previous step is done: they are free
-        sb["stage"].copy_(staged[i % copies][0], non_blocking=True)
-        sb["up"].record(s_copy)
-
-    def e2e_step(i):   # current stream: s_e2e
-        sb = slots_e2e[i % E2E_DEPTH]
-        s_e2e.wait_event(sb["up"])
-        sb["graphs"][i % copies].replay()
-        sb["run"].record(s_e2e)
-        with torch.cuda.stream(s_copy):
-            upload(i + 1)   # the next step's inputs go up while this step runs
-            s_copy.wait_event(sb["run"])
-            sb["h_out"].copy_(sb["out"], non_blocking=True)
-            sb["down"].record(s_copy)
-        sb["pending"] = True
-
-    def e2e_run(n):
-        with torch.cuda.stream(s_copy):
-            upload(0)
+    def e2e_run(first, n):
+        """Steps first .. first + n - 1; reads the outputs of steps first - 1 .. first + n - 2."""
         with torch.cuda.stream(s_e2e):
-            for i in range(n):
-                e2e_step(i)
-        for sb in slots_e2e:
-            read_back(sb)
+            for i in range(first, first + n):
+                e2e_graphs[i % period].replay()
+                slots_e2e[i % E2E_DEPTH]["done"].record(s_e2e)
+                if i >= 1:
+                    slots_e2e[(i - 1) % E2E_DEPTH]["done"].synchronize()
+                    checksum[0] += float(slots_e2e[(i - 2) % E2E_DEPTH]["h_out"][0, 0, 0])   # step i - 2's result
 
+    # prime the pipeline: the inputs of the first timed step are uploaded by the graph before it
+    with torch.cuda.stream(s_e2e):
+        slots_e2e[0]["stage"].copy_(staged[0][0])
+    e2e_run(0, 2 * period)
     e2e_steps = min(max(K, E2E_MIN_STEPS), E2E_MAX_STEPS)
-    e2e_run(E2E_DEPTH + 1)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
-    e2e_run(e2e_steps)
+    e2e_run(2 * period, e2e_steps)
     e2e_s = time.perf_counter() - t0
     torch.cuda.synchronize()
     if pa.pa_device_status() != 0:

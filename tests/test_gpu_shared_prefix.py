@@ -49,6 +49,8 @@ CASES = [
     (2, (10, 300, 0), 16, 4, 128, 256),             # the largest blocks: 512 shared tokens in two blocks
     (3, tuple(range(5, 75)), 12, 2, 128, 16),       # G = 6: row groups of 21 sequences (126 rows), two pairs
     (2, tuple(range(0, 70)), 32, 8, 64, 32),        # three row groups: the second pair holds one
+    (2, (5, 40, 0), 128, 1, 128, 16),               # G = 128: one sequence per row group, a half pair
+    (3, (7, 100), 64, 1, 64, 32),                   # G = 64: two sequences per row group
 ]
 
 

@@ -78,6 +78,28 @@ def test_static_scratch_matches_oracle_and_workspace_decode(case):
     assert pa.pa_device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("merge", ["scratch", "cluster"])
+def test_static_scratch_fp16(merge):
+    """fp16 query, caches and output, through the scratch and through a cluster."""
+    lens = (3000, 4164, 17, 900) if merge == "scratch" else (2000, 1999, 37, 1500, 2000, 64, 1024, 1777) * 2
+    Hq, Hkv, D, bs = 32, 8, 128, 16
+    plan = pa.pa_decode_plan(len(lens), Hq, Hkv, D, bs, max(lens), kv_dtype=pa.PA_F16, with_workspace=True)
+    assert plan["cluster_merge"] == (1 if merge == "cluster" else 0) and plan["num_splits"] > 1, plan
+    need = sum(workloads.cdiv(n, bs) for n in lens)
+    batch = workloads.make_batch("noalloc16", lens, Hq, Hkv, D, bs, need + 5, False, seed_values=930, f16=True)
+    want = oracle.paged_attention(batch.query, batch.k_cache, batch.v_cache, batch.block_tables,
+                                  batch.context_lens, batch.scale)
+    db = DeviceBatch(batch)
+    out = torch.full((len(lens), Hq, D), float("nan"), dtype=torch.float16, device="cuda")
+    pa.pa_decode_static_scratch(out, db.query, db.k_cache, db.v_cache, db.block_tables, db.context_lens,
+                                batch.max_context_len, batch.scale)
+    torch.cuda.synchronize()
+    g = out.float().cpu().numpy()
+    # rounding the output to fp16 adds at most half an ulp: 2^-11 relative
+    assert np.all(np.abs(g - want) <= ATOL + np.abs(want) * 2.0 ** -11)
+    assert pa.pa_device_status(clear=True) == 0
+
+
 def test_static_scratch_refuses_problem_larger_than_scratch():
     """A shape whose split (as pa_decode_plan reports it on this GPU) needs
     more than the fixed scratch is refused before any pointer is touched:

@@ -7,8 +7,8 @@
  * returns anything but PA_OK has enqueued nothing. Faults inside a kernel
  * surface at the caller's next synchronisation, as usual in CUDA.
  * State the library keeps (nothing else): one device status word per device
- * (pa_device_status), the fixed scratch of pa_decode_static_scratch, and the
- * second stream of pa_decode_shared_prefix (one per host thread and device).
+ * (pa_device_status) and the fixed scratch of pa_decode_static_scratch. Every
+ * kernel runs on the caller's stream; the library creates no stream or event.
  *
  * Conventions shared by every entry point
  *  - Pointers named *_cache, query, key, value, new_key, new_value, out,
@@ -261,12 +261,12 @@ PA_API pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *que
  *   Other arguments as pa_decode. Supported: bf16 or fp16 query and cache, head_dim
  *   64 or 128, block_size 8, 16, 32, 64, 128 or 256. With no whole tile
  *   shared this is pa_decode.
- *   Streams: the prefix pass runs on a second stream of the library's own,
- *   forked from `stream` and joined back into it by events, so the call stays
- *   ordered on `stream` and can be captured into a CUDA graph. That stream is
- *   created on the first call from each host thread on each device, and kept
- *   until the process exits. PA_PREFIX_OVERLAP=0 runs both passes on `stream`
- *   (no second stream is created).
+ *   Launches: three kernels on `stream` (capturable into a CUDA graph): the
+ *   rest-of-context decode, the prefix pass, the merge. The prefix pass is
+ *   launched as a programmatic dependent of the decode and starts on SMs the
+ *   decode frees; it does not read the decode's output and completes only
+ *   after the decode has, so the merge sees both. PA_PREFIX_OVERLAP=0 runs
+ *   the prefix pass first and the decode strictly after it.
  * ---------------------------------------------------------------------- */
 PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                                      int head_dim, int block_size,

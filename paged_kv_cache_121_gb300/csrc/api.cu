@@ -107,26 +107,13 @@ int heads_override() {
 }
 int heads_cap() { return heads_override() ? heads_override() : kMmaHeadsPerCta; }
 // PA_PREFIX_OVERLAP=0 runs the shared-prefix pass and the rest-of-context
-// decode one after the other on the caller's stream instead of side by side.
+// decode strictly one after the other instead of letting them overlap.
 bool prefix_overlap_enabled() {
     static const bool v = [] {
         const char *e = std::getenv("PA_PREFIX_OVERLAP");
         return !(e && std::strcmp(e, "0") == 0);
     }();
     return v;
-}
-
-// A second stream per (device, host thread), created on first use: the
-// shared-prefix pass runs there alongside the rest-of-context decode,
-// ordered against the caller's stream by events (capturable into a graph).
-cudaStream_t side_stream(int dev) {
-    thread_local cudaStream_t streams[kMaxDevices] = {};
-    if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess) {
-        cudaGetLastError();
-        streams[dev] = nullptr;
-    }
-    return streams[dev];
 }
 
 // PA_PREFIX_KERNEL=mma runs the shared-prefix pass on mma.sync instead of tcgen05.
@@ -150,6 +137,12 @@ int balance_mode() {
 //   PA_PREFIX_CTAS         CTAs the shared-prefix pass aims at (default: one per SM)
 int prefix_ctas_override() {
     static const int v = env_int("PA_PREFIX_CTAS", 1, 65536);
+    return v;
+}
+
+//   PA_PREFIX_GROUPS       row groups per CTA of the tcgen05 prefix pass (1 or 2)
+int prefix_groups_override() {
+    static const int v = env_int("PA_PREFIX_GROUPS", 1, 2);
     return v;
 }
 
@@ -631,7 +624,12 @@ PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms, bool tc
     if (tc) {
         pp.seqs_per_group = prefix_tc_max_rows() / group;
         pp.tc_groups = static_cast<int>(cdiv64(s.num_seqs, pp.seqs_per_group));
-        pp.groups_per_cta = pp.tc_groups >= 2 ? 2 : 1;
+        // head_dim 128: one row group per CTA. For the same number of CTAs that
+        // halves the chunks, so the partials written and merged, and each CTA
+        // runs twice the tiles through one setup. At head_dim 64, where a CTA
+        // with two groups sharing each K/V tile is small, two are faster.
+        pp.groups_per_cta = pp.tc_groups >= 2 && s.head_dim == 64 ? 2 : 1;
+        if (prefix_groups_override()) pp.groups_per_cta = std::min(pp.tc_groups, prefix_groups_override());
         pp.row_groups = static_cast<int>(cdiv64(pp.tc_groups, pp.groups_per_cta));
     } else {
         pp.row_groups = static_cast<int>(cdiv64(static_cast<int64_t>(s.num_seqs) * group, prefix_rows_per_cta()));
@@ -957,59 +955,39 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     float *max_logits = reinterpret_cast<float *>(ws + wl.ml_off);
     float *exp_sums = reinterpret_cast<float *>(ws + wl.count_off);
     cudaStream_t strm = as_stream(stream);
-    // The prefix pass and the rest-of-context decode write disjoint partitions:
-    // the prefix pass runs on a side stream forked from (and joined back into)
-    // the caller's stream, the rest on the caller's stream, then the merge.
-    cudaStream_t pstrm = strm;
-    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
-    if (prefix_overlap_enabled()) {
-        cudaStream_t side = side_stream(dev);
-        if (side && cudaEventCreateWithFlags(&fork_ev, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventCreateWithFlags(&join_ev, cudaEventDisableTiming) == cudaSuccess &&
-            cudaEventRecord(fork_ev, strm) == cudaSuccess && cudaStreamWaitEvent(side, fork_ev, 0) == cudaSuccess) {
-            pstrm = side;
-        } else {
-            cudaGetLastError();
-            if (fork_ev) cudaEventDestroy(fork_ev);
-            if (join_ev) cudaEventDestroy(join_ev);
-            fork_ev = join_ev = nullptr;
-        }
-    }
-    auto join = [&]() -> bool {   // the caller's stream waits for the side stream's work
-        if (pstrm == strm) return true;
-        const bool ok = cudaEventRecord(join_ev, pstrm) == cudaSuccess &&
-                        cudaStreamWaitEvent(strm, join_ev, 0) == cudaSuccess;
-        cudaEventDestroy(fork_ev);
-        cudaEventDestroy(join_ev);
-        pstrm = strm;
-        return ok;
-    };
-
-    // 1. the shared prefix, once for every row
-    PrefixParams pq;
-    std::memset(&pq, 0, sizeof pq);
-    pq.query = query;
-    pq.prefix_table = block_tables;   // row 0 holds the shared ids like every row
-    pq.context_lens = context_lens;
-    pq.tmp_out = tmp_out;
-    pq.max_logits = max_logits;
-    pq.exp_sums = exp_sums;
-    pq.status = status;
-    pq.num_seqs = num_seqs;
-    pq.num_heads = num_heads;
-    pq.num_kv_heads = num_kv_heads;
-    pq.head_dim = head_dim;
-    pq.group = num_heads / num_kv_heads;
-    pq.block_size = block_size;
-    pq.prefix_tokens = pp.prefix_tokens;
-    pq.chunk_tokens = pp.chunk_tokens;
-    pq.part_stride = pp.part_stride;
-    pq.scale_log2 = scale * kLog2e;
-    pq.kv_f16 = kv_dtype == PA_F16;
-    {
+    // The prefix pass and the rest-of-context decode write disjoint partitions.
+    // Both go on the caller's stream. With overlap on, the rest decode goes
+    // first and lets its dependent launch as soon as each of its CTAs starts;
+    // the prefix pass fills SMs as they free up and, at its very end, waits for
+    // the rest decode to complete, so that the merge (a dependent of the prefix
+    // pass) sees both. Without overlap the two run one after the other.
+    const bool overlap = prefix_overlap_enabled();
+    auto launch_prefix = [&]() -> pa_status {   // 1. the shared prefix, once for every row
+        PrefixParams pq;
+        std::memset(&pq, 0, sizeof pq);
+        pq.query = query;
+        pq.prefix_table = block_tables;   // row 0 holds the shared ids like every row
+        pq.context_lens = context_lens;
+        pq.tmp_out = tmp_out;
+        pq.max_logits = max_logits;
+        pq.exp_sums = exp_sums;
+        pq.status = status;
+        pq.num_seqs = num_seqs;
+        pq.num_heads = num_heads;
+        pq.num_kv_heads = num_kv_heads;
+        pq.head_dim = head_dim;
+        pq.group = num_heads / num_kv_heads;
+        pq.block_size = block_size;
+        pq.prefix_tokens = pp.prefix_tokens;
+        pq.chunk_tokens = pp.chunk_tokens;
+        pq.part_stride = pp.part_stride;
+        pq.scale_log2 = scale * kLog2e;
+        pq.kv_f16 = kv_dtype == PA_F16;
+        pq.after_rest = overlap ? 1 : 0;
         const dim3 grid(static_cast<unsigned>(pp.chunks), static_cast<unsigned>(num_kv_heads),
                         static_cast<unsigned>(pp.row_groups));
         CUtensorMap tk, tv;
+        pa_status err;
         if (pp.tc) {
             // boxes of one block (up to a 64-token tile), one 64-dim half, one head
             const int box = std::min(block_size, prefix_tc_tile_tokens());
@@ -1017,56 +995,51 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
             pq.seqs_per_group = pp.seqs_per_group;
             pq.row_groups = pp.tc_groups;
             CUtensorMap tq, to;
-            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1,
-                                     pq.kv_f16 != 0)) != PA_OK ||
-                (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1,
-                                     pq.kv_f16 != 0)) != PA_OK ||
-                (st = make_query_group_map(&tq, query, num_seqs, num_kv_heads, pq.group, head_dim,
-                                           pp.seqs_per_group, pq.kv_f16 != 0)) != PA_OK ||
-                (st = make_partials_store_map(&to, tmp_out, num_seqs, num_heads, pp.part_stride, head_dim, pq.group,
-                                              pp.seqs_per_group)) != PA_OK) {
-                join();
-                return st;
-            }
-            if (launch_prefix_tc(pq, pp.groups_per_cta, tk, tv, tq, to, grid, pstrm) != cudaSuccess) {
-                join();
-                return PA_ERR_CUDA;
-            }
-        } else {
-            const int box = decode_mma_box_tokens(block_size);
-            const int stage = prefix_stage_bytes(head_dim);
-            pq.ring_bytes = std::max(stage, std::min(kPrefixMaxRingBytes, ring_kb() * 1024) / stage * stage);
-            if ((st = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 0,
-                                     pq.kv_f16 != 0)) != PA_OK ||
-                (st = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 0,
-                                     pq.kv_f16 != 0)) != PA_OK) {
-                join();
-                return st;
-            }
-            if (launch_prefix_mma(pq, tk, tv, grid, pstrm) != cudaSuccess) {
-                join();
-                return PA_ERR_CUDA;
-            }
+            if ((err = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1,
+                                      pq.kv_f16 != 0)) != PA_OK ||
+                (err = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 1,
+                                      pq.kv_f16 != 0)) != PA_OK ||
+                (err = make_query_group_map(&tq, query, num_seqs, num_kv_heads, pq.group, head_dim,
+                                            pp.seqs_per_group, pq.kv_f16 != 0)) != PA_OK ||
+                (err = make_partials_store_map(&to, tmp_out, num_seqs, num_heads, pp.part_stride, head_dim,
+                                               pq.group, pp.seqs_per_group)) != PA_OK)
+                return err;
+            return launch_prefix_tc(pq, pp.groups_per_cta, tk, tv, tq, to, grid, strm) == cudaSuccess
+                       ? PA_OK : PA_ERR_CUDA;
         }
+        const int box = decode_mma_box_tokens(block_size);
+        const int stage = prefix_stage_bytes(head_dim);
+        pq.ring_bytes = std::max(stage, std::min(kPrefixMaxRingBytes, ring_kb() * 1024) / stage * stage);
+        if ((err = make_cache_map(&tk, k_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 0,
+                                  pq.kv_f16 != 0)) != PA_OK ||
+            (err = make_cache_map(&tv, v_cache, num_blocks, block_size, num_kv_heads, head_dim, box, 1, 0,
+                                  pq.kv_f16 != 0)) != PA_OK)
+            return err;
+        return launch_prefix_mma(pq, tk, tv, grid, strm) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    };
+    auto launch_rest = [&]() -> pa_status {   // 2. the rest of every context (the tokens past the shared ones)
+        DecodeParams p;
+        fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
+        p.tmp_out = tmp_out;
+        p.max_logits = max_logits;
+        p.exp_sums = exp_sums;
+        p.ntile = pp.suffix.ntile;
+        p.heads_per_cta = pp.suffix.heads_per_cta;
+        p.nsplit = pp.suffix.nsplit;
+        p.part_tokens = pp.suffix.part_tokens;
+        p.skip_tokens = pp.prefix_tokens;
+        p.part_stride = pp.part_stride;
+        // split-K partitions after the prefix chunks, then the merge
+        p.part_offset = pp.chunks;
+        p.mode = kModeSplitK;
+        p.trigger_early = overlap ? 1 : 0;
+        return launch_decode(s, p, kv_dtype, true, dev, strm);
+    };
+    if (overlap) {
+        if ((st = launch_rest()) != PA_OK || (st = launch_prefix()) != PA_OK) return st;
+    } else {
+        if ((st = launch_prefix()) != PA_OK || (st = launch_rest()) != PA_OK) return st;
     }
-    // 2. the rest of every context (the tokens past the shared ones)
-    DecodeParams p;
-    fill_common(p, s, query, q_dtype, k_cache, v_cache, block_tables, context_lens, scale);
-    p.tmp_out = tmp_out;
-    p.max_logits = max_logits;
-    p.exp_sums = exp_sums;
-    p.ntile = pp.suffix.ntile;
-    p.heads_per_cta = pp.suffix.heads_per_cta;
-    p.nsplit = pp.suffix.nsplit;
-    p.part_tokens = pp.suffix.part_tokens;
-    p.skip_tokens = pp.prefix_tokens;
-    p.part_stride = pp.part_stride;
-    // split-K partitions after the prefix chunks, then the merge
-    p.part_offset = pp.chunks;
-    p.mode = kModeSplitK;
-    st = launch_decode(s, p, kv_dtype, true, dev, strm);
-    if (!join() && st == PA_OK) st = PA_ERR_CUDA;
-    if (st != PA_OK) return st;
     // 3. merge all partitions of every row
     const cudaError_t e = launch_lse_merge(out, static_cast<int>(out_dtype), tmp_out, max_logits, exp_sums,
                                            context_lens, num_seqs, num_heads, head_dim, pp.part_stride, 0, sms,

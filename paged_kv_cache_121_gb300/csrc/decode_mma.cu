@@ -227,6 +227,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int b = blockIdx.z;
     const int rows = min(kRowsPerTile, p.group - tile * kRowsPerTile);
     grid_dependency_wait();   // the previous kernel on the stream (e.g. the scatter) is complete
+    if (p.trigger_early) grid_dependents_launch();
     const SeqWork w = seq_work(p, b, part);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // (one instantiation per epilogue keeps the other's registers out of the loop)

@@ -57,6 +57,8 @@ struct DecodeParams {
     int kv_f16;          // 16-bit query and caches are fp16 (else bf16)
     const void *append_key;     // [num_seqs, Hkv, D] or null: the step's new token of sequence b,
     const void *append_value;   //   written to position context_lens[b] - 1 before it is read
+    int trigger_early;          // let the next kernel be scheduled right after the dependency wait
+                                // (it must not read this launch's output before its own end)
     float scale_log2;    // scale * log2(e): scores are kept in base-2 units
 };
 
@@ -127,6 +129,10 @@ struct PrefixParams {
     int kv_f16;                   // query and caches are fp16 (else bf16)
     int seqs_per_group;           // tcgen05 pass: whole sequences per row group (rows = this x group)
     int row_groups;               // tcgen05 pass: row groups of the batch
+    int after_rest;               // launched early behind the rest-of-context decode (which reads
+                                  // nothing of this pass): no wait at the start, which that decode
+                                  // already made; a wait for it at the end, so that this grid's
+                                  // completion implies the decode's
     float scale_log2;
 };
 

@@ -77,9 +77,12 @@ struct TcCfg {
     static constexpr int kPOffset = kGroups * kQBytes;
     static constexpr int kRingOffset = kPOffset + 2 * kGroups * kPBytes;
     static size_t smem_bytes(int ring);
-    static int min_ring_bytes() {   // the staged output must fit in P + ring
+    // At least two stages: tile i + 1's Q.K^T is issued before tile i's P.V,
+    // which frees tile i's stage, so one stage would wait on itself. And the
+    // staged output must fit in P + ring.
+    static int min_ring_bytes() {
         const int need = kGroups * kOutBytes - 2 * kGroups * kPBytes;
-        return need > kStageBytes ? need : kStageBytes;
+        return need > 2 * kStageBytes ? need : 2 * kStageBytes;
     }
     static int max_ring_bytes();    // whole stages within the shared memory of one CTA
 };
@@ -164,7 +167,7 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tma_prefetch_desc(&tmap_v);
         tma_prefetch_desc(&tmap_o);
     }
-    grid_dependency_wait();
+    if (!p.after_rest) grid_dependency_wait();
     const int chunk = blockIdx.x, kvh = blockIdx.y;
     const int grp0 = blockIdx.z * kGroups;                      // this CTA's first row group
     const int ngrp = min(kGroups, p.row_groups - grp0);         // row groups with rows (>= 1)
@@ -453,6 +456,7 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+    if (p.after_rest) grid_dependency_wait();   // this grid completes after the rest-of-context decode
 }
 
 template <int D, int kGroups, bool kF16>

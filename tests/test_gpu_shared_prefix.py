@@ -4,6 +4,14 @@ log-sum-exp, must give plain paged attention ("PagedAttention: KV cache
 virtual memory", "Copy-on-write: when two requests share a prefix"; "Paged
 Attention: Virtual Memory for the KV Cache", "Sharing a prefix: one copy for
 many requests")."""
+import json
+import os
+import subprocess
+import sys
+
+if __name__ == "__main__":   # the child process: the repo root, as conftest gives pytest
+    sys.path[:0] = [os.path.dirname(os.path.dirname(os.path.abspath(__file__)))]
+
 import numpy as np
 import pytest
 import torch
@@ -47,8 +55,8 @@ CASES = [
     (9, (12, 250, 31), 24, 12, 128, 64),            # 12 KV heads
     (4, (1000, 2000, 5, 700), 32, 8, 128, 16),      # long rests: split, partitions merged by the merge kernel
     (2, (10, 300, 0), 16, 4, 128, 256),             # the largest blocks: 512 shared tokens in two blocks
-    (3, tuple(range(5, 75)), 12, 2, 128, 16),       # G = 6: row groups of 21 sequences (126 rows), two pairs
-    (2, tuple(range(0, 70)), 32, 8, 64, 32),        # three row groups: the second pair holds one
+    (3, tuple(range(5, 75)), 12, 2, 128, 16),       # G = 6: four row groups of 21 sequences (126 rows)
+    (2, tuple(range(0, 70)), 32, 8, 64, 32),        # D 64, three row groups, two per CTA: the second pair holds one
     (2, (5, 40, 0), 128, 1, 128, 16),               # G = 128: one sequence per row group, a half pair
     (3, (7, 100), 64, 1, 64, 32),                   # G = 64: two sequences per row group
 ]
@@ -145,9 +153,9 @@ def test_shared_prefix_cow_workload(prefix_len):
 
 
 def test_shared_prefix_in_a_cuda_graph_matches_eager():
-    """The prefix pass runs on a side stream forked from the caller's stream;
-    captured into a CUDA graph (as a serving loop would) and replayed, the
-    call gives the eager result."""
+    """The call's three kernels (rest-of-context decode, prefix pass launched
+    as its programmatic dependent, merge) captured into a CUDA graph (as a
+    serving loop would) and replayed give the eager result."""
     batch = workloads.shared_prefix_batch("sp", 32, tuple(range(5, 400, 25)), 32, 8, 128, 32, seed_values=830)
     db = DeviceBatch(batch)
     n = pa.pa_decode_shared_prefix_workspace_size(batch.num_seqs, 32, 8, 128, 32, batch.max_context_len, 32)
@@ -169,3 +177,43 @@ def test_shared_prefix_in_a_cuda_graph_matches_eager():
     assert torch.equal(out, eager)
     assert max_err(out, oracle_out(batch)) <= ATOL
     assert pa.pa_device_status(clear=True) == 0
+
+
+def child_smallest_ring():
+    """Run with the smallest ring budget (PA_DECODE_RING_KB=16) and few
+    prefix CTAs (PA_PREFIX_CTAS=16), so that each CTA of the tcgen05 pass
+    streams many tiles through its ring: head_dim 128 with 24 and with 80
+    sequences (one or, under PA_PREFIX_GROUPS=2, two row groups per CTA), and
+    head_dim 64 with 80 sequences (two row groups per CTA)."""
+    errs = []
+    for seed, suffix, d in ((850, tuple(range(3, 27)), 128), (851, tuple(range(0, 80)), 128),
+                            (852, tuple(range(0, 80)), 64)):
+        batch = workloads.shared_prefix_batch("ring", 40, suffix, 32, 8, d, 32, seed_values=seed)
+        db = DeviceBatch(batch)
+        n = pa.pa_decode_shared_prefix_workspace_size(batch.num_seqs, 32, 8, d, 32, batch.max_context_len, 40)
+        ws = torch.zeros(max(n, 1), dtype=torch.uint8, device="cuda")
+        out = torch.empty((batch.num_seqs, 32, d), dtype=torch.float32, device="cuda")
+        pa.pa_decode_shared_prefix(out, db.query, db.k_cache, db.v_cache, db.block_tables, db.context_lens,
+                                   batch.max_context_len, 40, batch.scale, ws)
+        torch.cuda.synchronize()
+        errs.append(max_err(out, oracle_out(batch)))
+    print(json.dumps({"errs": errs, "status": pa.pa_device_status(clear=True)}))
+
+
+@pytest.mark.parametrize("groups", ["default", "2"])
+def test_shared_prefix_with_the_smallest_ring(groups):
+    """A ring of one stage would wait on itself (tile i + 1's Q.K^T is issued
+    before tile i's P.V frees its stage); the pass takes two stages at least
+    whatever the budget. Knobs are read once per process: a child runs it."""
+    env = dict(os.environ, PA_DECODE_RING_KB="16", PA_PREFIX_CTAS="16")
+    if groups != "default":
+        env["PA_PREFIX_GROUPS"] = groups
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "child"], env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["status"] == 0 and max(res["errs"]) <= ATOL, res
+
+
+if __name__ == "__main__" and sys.argv[1:] == ["child"]:
+    child_smallest_ring()

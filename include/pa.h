@@ -262,11 +262,13 @@ PA_API pa_status pa_decode_append(void *out, pa_dtype out_dtype, const void *que
  *   64 or 128, block_size 8, 16, 32, 64, 128 or 256. With no whole tile
  *   shared this is pa_decode.
  *   Launches: three kernels on `stream` (capturable into a CUDA graph): the
- *   rest-of-context decode, the prefix pass, the merge. The prefix pass is
- *   launched as a programmatic dependent of the decode and starts on SMs the
- *   decode frees; it does not read the decode's output and completes only
- *   after the decode has, so the merge sees both. PA_PREFIX_OVERLAP=0 runs
- *   the prefix pass first and the decode strictly after it.
+ *   prefix pass, the rest-of-context decode, the merge. The decode is
+ *   launched as a programmatic dependent of the prefix pass and runs beside
+ *   it, on the SMs the pass's plan leaves free; neither reads the other's
+ *   output, and the decode completes only after the pass has, so the merge
+ *   sees both. PA_PREFIX_ORDER=rest puts the decode first (the pass then
+ *   fills the SMs it frees); PA_PREFIX_OVERLAP=0 runs the two one after the
+ *   other. With PA_PREFIX_KERNEL=mma the decode goes first.
  * ---------------------------------------------------------------------- */
 PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                                      int head_dim, int block_size,

@@ -40,6 +40,12 @@ constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
 constexpr int kMinPrefixChunk = 64;   // tokens per chunk of the shared-prefix pass, at least
 constexpr int kMinRestSplitTokens = 64;   // partitions of the rest of a shared-prefix context, at least
 constexpr int kRestCtasPerSm = 3;         // the rest's split aims past one wave: CTAs of short rests end early
+// The SM share of a prefix pass that runs first (measured over fourteen
+// copy-on-write shapes on GB300): one unit of its work (a 64-token tile of
+// one 128-row group and KV head) weighs as much as this many MB of the
+// rest-of-context decode's K/V; at this share or above it takes every SM.
+constexpr double kPrefixUnitMB = 0.18;
+constexpr double kPrefixAllSmsFrac = 0.85;
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int *> g_status_addr[kMaxDevices];
@@ -141,6 +147,15 @@ int prefix_ctas_override() {
 }
 
 //   PA_PREFIX_GROUPS       row groups per CTA of the tcgen05 prefix pass (1 or 2)
+//   PA_PREFIX_ORDER        "rest": the rest-of-context decode first, the prefix pass
+//                          behind it (default: the prefix pass first)
+bool prefix_first_enabled() {
+    static const bool v = [] {
+        const char *e = std::getenv("PA_PREFIX_ORDER");
+        return !(e && std::strcmp(e, "rest") == 0);
+    }();
+    return v;
+}
 int prefix_groups_override() {
     static const int v = env_int("PA_PREFIX_GROUPS", 1, 2);
     return v;
@@ -636,9 +651,26 @@ PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms, bool tc
     }
     if (P > 0) {
         const int64_t per_chunk = static_cast<int64_t>(s.num_kv_heads) * pp.row_groups;
-        const int64_t cap = prefix_ctas_override() ? prefix_ctas_override()
-                                                   : static_cast<int64_t>(sms) * (tc ? 1 : kCtasPerSmMma);
+        int64_t cap = prefix_ctas_override() ? prefix_ctas_override()
+                                             : static_cast<int64_t>(sms) * (tc ? 1 : kCtasPerSmMma);
         int64_t chunks = std::max<int64_t>(1, cap / per_chunk);
+        if (tc && !prefix_ctas_override() && prefix_first_enabled()) {
+            // The prefix pass goes first and holds its SMs (one CTA each) while
+            // the rest-of-context decode runs on the others: give it a share of
+            // the SMs in proportion to its work, the rest's bytes at the largest
+            // lengths against the pass's (64-token tile x 128-row group x KV
+            // head) units, each worth kPrefixUnitMB of rest; all of them when
+            // the rest is small.
+            const double units = static_cast<double>(P / tile) * s.num_kv_heads * pp.tc_groups * s.head_dim / 128.0;
+            const double rest_mb = static_cast<double>(s.num_seqs) * std::max<int64_t>(0, s.max_ctx - P) *
+                                   s.num_kv_heads * s.head_dim * 4 / 1e6;
+            const double frac = units * kPrefixUnitMB / (units * kPrefixUnitMB + rest_mb);
+            if (frac < kPrefixAllSmsFrac) {
+                const int64_t share = std::max<int64_t>(1, std::llround(sms * frac));
+                chunks = std::max<int64_t>(1, std::min<int64_t>((share + per_chunk / 2) / per_chunk,
+                                                                std::max<int64_t>(1, sms / per_chunk)));
+            }
+        }
         chunks = std::min<int64_t>(chunks, std::max<int64_t>(1, P / std::max(kMinPrefixChunk, tile)));
         chunks = std::min<int64_t>(chunks, kMaxSplits);
         const int64_t tiles = P / tile;
@@ -955,13 +987,14 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
     float *max_logits = reinterpret_cast<float *>(ws + wl.ml_off);
     float *exp_sums = reinterpret_cast<float *>(ws + wl.count_off);
     cudaStream_t strm = as_stream(stream);
-    // The prefix pass and the rest-of-context decode write disjoint partitions.
-    // Both go on the caller's stream. With overlap on, the rest decode goes
-    // first and lets its dependent launch as soon as each of its CTAs starts;
-    // the prefix pass fills SMs as they free up and, at its very end, waits for
-    // the rest decode to complete, so that the merge (a dependent of the prefix
-    // pass) sees both. Without overlap the two run one after the other.
+    // The prefix pass and the rest-of-context decode write disjoint partitions
+    // and read nothing of each other's: they overlap as a pair (PairRole) on
+    // the caller's stream, then the merge, the second's dependent, sees both.
+    // The tcgen05 pass goes first, on the share of SMs its plan gave it, and
+    // the decode runs on the others; the mma.sync pass goes second, into SMs
+    // the decode frees. Without overlap the two run one after the other.
     const bool overlap = prefix_overlap_enabled();
+    const bool prefix_first = prefix_first_enabled() && pp.tc;
     auto launch_prefix = [&]() -> pa_status {   // 1. the shared prefix, once for every row
         PrefixParams pq;
         std::memset(&pq, 0, sizeof pq);
@@ -983,7 +1016,7 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
         pq.part_stride = pp.part_stride;
         pq.scale_log2 = scale * kLog2e;
         pq.kv_f16 = kv_dtype == PA_F16;
-        pq.after_rest = overlap ? 1 : 0;
+        pq.pair_role = !overlap ? kPairNone : prefix_first ? kPairFirst : kPairSecond;
         const dim3 grid(static_cast<unsigned>(pp.chunks), static_cast<unsigned>(num_kv_heads),
                         static_cast<unsigned>(pp.row_groups));
         CUtensorMap tk, tv;
@@ -1032,10 +1065,10 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
         // split-K partitions after the prefix chunks, then the merge
         p.part_offset = pp.chunks;
         p.mode = kModeSplitK;
-        p.trigger_early = overlap ? 1 : 0;
+        p.pair_role = !overlap ? kPairNone : prefix_first ? kPairSecond : kPairFirst;
         return launch_decode(s, p, kv_dtype, true, dev, strm);
     };
-    if (overlap) {
+    if (overlap && !prefix_first) {
         if ((st = launch_rest()) != PA_OK || (st = launch_prefix()) != PA_OK) return st;
     } else {
         if ((st = launch_prefix()) != PA_OK || (st = launch_rest()) != PA_OK) return st;

@@ -226,8 +226,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tile = blockIdx.y % p.ntile;
     const int b = blockIdx.z;
     const int rows = min(kRowsPerTile, p.group - tile * kRowsPerTile);
-    grid_dependency_wait();   // the previous kernel on the stream (e.g. the scatter) is complete
-    if (p.trigger_early) grid_dependents_launch();
+    // the previous kernel on the stream (e.g. the scatter) is complete
+    if (p.pair_role != kPairSecond) grid_dependency_wait();
+    if (p.pair_role == kPairFirst) grid_dependents_launch();
+    // second of a pair: one CTA outlives the first kernel (the others need not hold their SMs)
+    const bool tie = p.pair_role == kPairSecond && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
     const SeqWork w = seq_work(p, b, part);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // (one instantiation per epilogue keeps the other's registers out of the loop)
@@ -237,6 +240,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int gh = hgrp * hpc + warp;
             warp_write_empty<D>(p, b, gh * p.group + tile * kRowsPerTile, part, rows, w.nparts, lane);
         }
+        if (tie) grid_dependency_wait();
         return;
     }
     // (in a cluster every CTA takes part in the exchange, an empty partition included)
@@ -486,6 +490,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         __syncthreads();
         cluster_exchange_merge<D>(p, st, reinterpret_cast<float *>(smem), b, hgrp, tile, rows, warp, lane);
     }
+    if (tie) grid_dependency_wait();
 }
 
 template <int D, int TT, int kLoad, bool kF16>

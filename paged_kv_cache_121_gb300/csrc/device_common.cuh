@@ -23,6 +23,16 @@ enum DecodeMode : int { kModeFinal = 0, kModeSplitK = 1 };
 enum StatusCode : int { kStatusTimeout = 5 };
 
 // Everything a decode launch needs; passed by value.
+// Two kernels that read nothing of each other's output (the shared-prefix
+// pass and the rest-of-context decode) overlap through programmatic
+// dependent launch. The first waits for the stream as usual, then lets the
+// second launch at once: the second is scheduled as soon as every CTA of the
+// first has started, so no CTA ever waits on one that is not resident. The
+// second skips the start-of-kernel wait (the first already made it) and
+// instead waits for the first before it exits, so that its completion, which
+// the next kernel waits for, implies the first's.
+enum PairRole : int { kPairNone = 0, kPairFirst = 1, kPairSecond = 2 };
+
 struct DecodeParams {
     const void *query;
     const void *k_cache;
@@ -57,8 +67,7 @@ struct DecodeParams {
     int kv_f16;          // 16-bit query and caches are fp16 (else bf16)
     const void *append_key;     // [num_seqs, Hkv, D] or null: the step's new token of sequence b,
     const void *append_value;   //   written to position context_lens[b] - 1 before it is read
-    int trigger_early;          // let the next kernel be scheduled right after the dependency wait
-                                // (it must not read this launch's output before its own end)
+    int pair_role;              // PairRole: one of two overlapped kernels, or neither
     float scale_log2;    // scale * log2(e): scores are kept in base-2 units
 };
 
@@ -129,10 +138,7 @@ struct PrefixParams {
     int kv_f16;                   // query and caches are fp16 (else bf16)
     int seqs_per_group;           // tcgen05 pass: whole sequences per row group (rows = this x group)
     int row_groups;               // tcgen05 pass: row groups of the batch
-    int after_rest;               // launched early behind the rest-of-context decode (which reads
-                                  // nothing of this pass): no wait at the start, which that decode
-                                  // already made; a wait for it at the end, so that this grid's
-                                  // completion implies the decode's
+    int pair_role;                // PairRole: one of two overlapped kernels, or neither
     float scale_log2;
 };
 

@@ -58,7 +58,8 @@ prefix_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     __shared__ int s_abort;
     __shared__ int s_issued;
 
-    if (!p.after_rest) grid_dependency_wait();
+    if (p.pair_role != kPairSecond) grid_dependency_wait();
+    if (p.pair_role == kPairFirst) grid_dependents_launch();
     const int chunk = blockIdx.x;
     const int g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -221,7 +222,7 @@ prefix_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             if (!mbar_wait(smem_addr(&bars[s]), k_last & 1)) record_status(p.status, kStatusTimeout);
         }
     }
-    if (p.after_rest) grid_dependency_wait();   // this grid completes after the rest-of-context decode
+    if (p.pair_role == kPairSecond) grid_dependency_wait();   // this grid completes after the first
 }
 
 template <int D, bool kPairs, bool kF16>

@@ -167,7 +167,8 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tma_prefetch_desc(&tmap_v);
         tma_prefetch_desc(&tmap_o);
     }
-    if (!p.after_rest) grid_dependency_wait();
+    if (p.pair_role != kPairSecond) grid_dependency_wait();
+    if (p.pair_role == kPairFirst) grid_dependents_launch();
     const int chunk = blockIdx.x, kvh = blockIdx.y;
     const int grp0 = blockIdx.z * kGroups;                      // this CTA's first row group
     const int ngrp = min(kGroups, p.row_groups - grp0);         // row groups with rows (>= 1)
@@ -357,6 +358,17 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             const float alpha = fast_exp2(m - m_new);
             m = m_new;
             l *= alpha;
+            // P in registers first, in the type of V (high part and residual):
+            // this overlaps the previous tile's P.V, which still reads the buffer
+            uint32_t hi[kTcTile / 2], lo[kTcTile / 2];
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < kTcTile / 2; ++e) {
+                const float p0 = fast_exp2(s[2 * e] - m), p1 = fast_exp2(s[2 * e + 1] - m);
+                l4[e & 3] += p0 + p1;
+                split_x2<kF16>(p0, p1, hi[e], lo[e]);
+            }
+            l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             if (i >= 1) {
                 // the previous tile's P.V has read the P buffer and landed in O
                 if (!tc_wait(p, bars, &bars->pv_done[g], (i - 1) & 1)) { ok = false; break; }
@@ -373,21 +385,12 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 }
             }
             unsigned char *hi_b = p_hi(g), *lo_b = p_lo(g);
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {   // 8 tokens per 16-byte chunk
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(s[8 * c + 2 * e] - m), p1 = fast_exp2(s[8 * c + 2 * e + 1] - m);
-                    l4[e] += p0 + p1;
-                    split_x2<kF16>(p0, p1, hi[e], lo[e]);   // P in the type of V
-                }
+            for (int c = 0; c < 8; ++c) {   // 8 tokens per 16-byte chunk, at chunk c ^ (row % 8)
                 const int pos = R * 128 + ((c ^ (R & 7)) << 4);
-                *reinterpret_cast<uint4 *>(hi_b + pos) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(lo_b + pos) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                *reinterpret_cast<uint4 *>(hi_b + pos) = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+                *reinterpret_cast<uint4 *>(lo_b + pos) = make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
             }
-            l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -456,7 +459,7 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
-    if (p.after_rest) grid_dependency_wait();   // this grid completes after the rest-of-context decode
+    if (p.pair_role == kPairSecond) grid_dependency_wait();   // this grid completes after the first
 }
 
 template <int D, int kGroups, bool kF16>

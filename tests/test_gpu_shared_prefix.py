@@ -179,16 +179,14 @@ def test_shared_prefix_in_a_cuda_graph_matches_eager():
     assert pa.pa_device_status(clear=True) == 0
 
 
-def child_smallest_ring():
-    """Run with the smallest ring budget (PA_DECODE_RING_KB=16) and few
-    prefix CTAs (PA_PREFIX_CTAS=16), so that each CTA of the tcgen05 pass
-    streams many tiles through its ring: head_dim 128 with 24 and with 80
-    sequences (one or, under PA_PREFIX_GROUPS=2, two row groups per CTA), and
-    head_dim 64 with 80 sequences (two row groups per CTA)."""
+def child_cases():
+    """Three batches through pa_decode_shared_prefix under the knobs the parent
+    set: head_dim 128 with 24 and with 80 sequences (one row group per CTA,
+    or two under PA_PREFIX_GROUPS=2), and head_dim 64 with 80 (two)."""
     errs = []
     for seed, suffix, d in ((850, tuple(range(3, 27)), 128), (851, tuple(range(0, 80)), 128),
                             (852, tuple(range(0, 80)), 64)):
-        batch = workloads.shared_prefix_batch("ring", 40, suffix, 32, 8, d, 32, seed_values=seed)
+        batch = workloads.shared_prefix_batch("knob", 40, suffix, 32, 8, d, 32, seed_values=seed)
         db = DeviceBatch(batch)
         n = pa.pa_decode_shared_prefix_workspace_size(batch.num_seqs, 32, 8, d, 32, batch.max_context_len, 40)
         ws = torch.zeros(max(n, 1), dtype=torch.uint8, device="cuda")
@@ -200,14 +198,24 @@ def child_smallest_ring():
     print(json.dumps({"errs": errs, "status": pa.pa_device_status(clear=True)}))
 
 
-@pytest.mark.parametrize("groups", ["default", "2"])
-def test_shared_prefix_with_the_smallest_ring(groups):
-    """A ring of one stage would wait on itself (tile i + 1's Q.K^T is issued
-    before tile i's P.V frees its stage); the pass takes two stages at least
-    whatever the budget. Knobs are read once per process: a child runs it."""
-    env = dict(os.environ, PA_DECODE_RING_KB="16", PA_PREFIX_CTAS="16")
-    if groups != "default":
-        env["PA_PREFIX_GROUPS"] = groups
+KNOBS = {
+    # the smallest ring budget and few prefix CTAs, so that each CTA streams many
+    # tiles through its ring: a ring of one stage would wait on itself (tile
+    # i + 1's Q.K^T is issued before tile i's P.V frees its stage), so the
+    # tcgen05 pass takes two stages at least whatever the budget
+    "smallest_ring": {"PA_DECODE_RING_KB": "16", "PA_PREFIX_CTAS": "16"},
+    "smallest_ring_two_groups": {"PA_DECODE_RING_KB": "16", "PA_PREFIX_CTAS": "16", "PA_PREFIX_GROUPS": "2"},
+    # the other orders of the two passes: the decode first, the prefix pass as
+    # its programmatic dependent; or one after the other
+    "rest_first": {"PA_PREFIX_ORDER": "rest"},
+    "serial": {"PA_PREFIX_OVERLAP": "0"},
+}
+
+
+@pytest.mark.parametrize("knobs", sorted(KNOBS))
+def test_shared_prefix_under_knobs(knobs):
+    """Knobs are read once per process: a child process runs the batches."""
+    env = dict(os.environ, **KNOBS[knobs])
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "child"], env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
@@ -216,4 +224,4 @@ def test_shared_prefix_with_the_smallest_ring(groups):
 
 
 if __name__ == "__main__" and sys.argv[1:] == ["child"]:
-    child_smallest_ring()
+    child_cases()

@@ -33,6 +33,7 @@ constexpr int kMmaRingKiB = 96;       // shared-memory ring per tensor-core CTA:
                                       // cluster merges the split,
 constexpr int kSplitRingKiB = 64;     // two when the split goes through the workspace (measured on
                                       // GB300: 4 x 32 K tokens 87.0-87.5 us against 89.1-89.5 with three)
+constexpr int kPrefixTcRingKiB = 192;  // tcgen05 prefix pass: as many stages as fit beside Q and P
 constexpr int kBalancedHeadsPerCta = 8;   // ragged-balanced decode: every KV head of a group in one CTA,
 constexpr int kBalancedCtasPerSm = 1;     //   one CTA per SM,
 constexpr int kBalancedRingKiB = 132;     //   two 64 KiB stages (93.6 us against 94.0 with three)
@@ -1024,7 +1025,8 @@ PA_API pa_status pa_decode_shared_prefix(void *out, pa_dtype out_dtype, const vo
         if (pp.tc) {
             // boxes of one block (up to a 64-token tile), one 64-dim half, one head
             const int box = std::min(block_size, prefix_tc_tile_tokens());
-            pq.ring_bytes = prefix_tc_ring_bytes(head_dim, pp.groups_per_cta, ring_kb() * 1024);
+            pq.ring_bytes = prefix_tc_ring_bytes(head_dim, pp.groups_per_cta,
+                                                 (ring_override_kb() ? ring_override_kb() : kPrefixTcRingKiB) * 1024);
             pq.seqs_per_group = pp.seqs_per_group;
             pq.row_groups = pp.tc_groups;
             CUtensorMap tq, to;

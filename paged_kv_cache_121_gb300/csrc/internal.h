@@ -28,7 +28,7 @@ cudaError_t launch_prefix_mma(const PrefixParams &p, const CUtensorMap &tmap_k, 
                               dim3 grid, cudaStream_t stream);
 // Shared-prefix pass on tcgen05 (prefix_tc.cu): grid (chunks, Hkv, cdiv(row groups, groups_per_cta)).
 // A row group is floor(128 / G) whole sequences x their G query heads (G <= 128).
-constexpr int kTcMaxRingBytes = 128 * 1024;
+constexpr int kTcMaxRingBytes = 192 * 1024;
 constexpr int kTcChunkBlocks = 256;   // most block ids one chunk of the tcgen05 pass may span
 int prefix_tc_max_rows();             // rows of a row group at most (tensor-memory lanes)
 int prefix_tc_tile_tokens();

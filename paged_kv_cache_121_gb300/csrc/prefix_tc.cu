@@ -239,7 +239,7 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                     tma_load_5d(smem_addr(q_s + (g * C::kHalves + h) * (kTcLanes * 128)), &tmap_q, 0, h, 0, kvh,
                                 (grp0 + g) * spg, qf, q_policy);
             policy = l2_policy_evict_last();   // every row group reads the prefix
-            preissued = min(nstages, ntiles);
+            preissued = min(1, ntiles);   // the producer loop issues the next ones after the sync
             for (int i = 0; i < preissued; ++i) issue_tile(i);
             bars->issued = preissued;
         }
@@ -341,17 +341,33 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             if (lane == 0) mbar_arrive(smem_addr(&bars->s_free[g][b]));
             const int t0 = tok_begin + i * kTcTile;
             const int valid = min(kTcTile, max(0, len - t0));
+            // Tokens past a live row's length only occur when the shared blocks
+            // are shorter than a context (outside the contract): masked then.
+            // Rows past the batch read a zero Q, so their scores are finite;
+            // their outputs are never stored. The largest scaled score is the
+            // scale times the largest raw score (the smallest, for a negative
+            // scale); masked scores scale to -inf.
+            const bool up = sl2 >= 0.f;
+            if (__any_sync(0xffffffffu, live && valid < kTcTile)) {
+#pragma unroll
+                for (int j = 0; j < kTcTile; ++j) s[j] = j < valid ? s[j] : up ? -INFINITY : INFINITY;
+            }
             // (eight partial maxima and four partial sums: short dependency chains)
             float mx8[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) mx8[j] = -INFINITY;
+            for (int j = 0; j < 8; ++j) mx8[j] = s[j];
+            if (up) {
 #pragma unroll
-            for (int j = 0; j < kTcTile; ++j) {
-                s[j] = j < valid ? s[j] * sl2 : -INFINITY;
-                mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
+                for (int j = 8; j < kTcTile; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], s[j]);
+            } else {
+#pragma unroll
+                for (int j = 8; j < kTcTile; ++j) mx8[j & 7] = fminf(mx8[j & 7], s[j]);
             }
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mx8[j] = up ? fmaxf(mx8[j], mx8[j + 4]) : fminf(mx8[j], mx8[j + 4]);
+            const float e01 = up ? fmaxf(mx8[0], mx8[1]) : fminf(mx8[0], mx8[1]);
+            const float e23 = up ? fmaxf(mx8[2], mx8[3]) : fminf(mx8[2], mx8[3]);
+            const float mx = sl2 * (up ? fmaxf(e01, e23) : fminf(e01, e23));
             t = fmaxf(t, mx);
             const bool need = mx > m + kTcSlack;
             const float m_new = need ? fmaxf(m, mx) : m;
@@ -363,8 +379,8 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             uint32_t hi[kTcTile / 2], lo[kTcTile / 2];
             float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < kTcTile / 2; ++e) {
-                const float p0 = fast_exp2(s[2 * e] - m), p1 = fast_exp2(s[2 * e + 1] - m);
+            for (int e = 0; e < kTcTile / 2; ++e) {   // 2^(s * scale - m): one fma and one ex2
+                const float p0 = fast_exp2(fmaf(s[2 * e], sl2, -m)), p1 = fast_exp2(fmaf(s[2 * e + 1], sl2, -m));
                 l4[e & 3] += p0 + p1;
                 split_x2<kF16>(p0, p1, hi[e], lo[e]);
             }

@@ -152,6 +152,16 @@ def test_shared_prefix_cow_workload(prefix_len):
     assert max_err(out, oracle_out(batch)) <= ATOL
 
 
+def test_shared_prefix_negative_scale():
+    """A negative softmax scale (the largest scaled score then comes from the
+    smallest raw one), both passes, against the oracle."""
+    for d, seed in ((128, 870), (64, 871)):
+        batch = workloads.shared_prefix_batch("neg", 12, tuple(range(0, 300, 7)), 32, 8, d, 16, seed_values=seed)
+        batch.scale = -0.7 / np.sqrt(d)
+        out = run_shared(DeviceBatch(batch), 12)
+        assert max_err(out, oracle_out(batch)) <= ATOL
+
+
 def test_shared_prefix_in_a_cuda_graph_matches_eager():
     """The call's three kernels (rest-of-context decode, prefix pass launched
     as its programmatic dependent, merge) captured into a CUDA graph (as a

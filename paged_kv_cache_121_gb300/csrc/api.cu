@@ -40,12 +40,12 @@ constexpr int kBalancedRingKiB = 132;     //   two 64 KiB stages (93.6 us agains
 constexpr int kMinSplitTokens = 256;  // do not split a context finer than this
 constexpr int kMinPrefixChunk = 64;   // tokens per chunk of the shared-prefix pass, at least
 constexpr int kMinRestSplitTokens = 64;   // partitions of the rest of a shared-prefix context, at least
-constexpr int kRestCtasPerSm = 3;         // the rest's split aims past one wave: CTAs of short rests end early
+constexpr int kRestCtasPerSm = 2;         // the rest's split: two CTAs per SM (it runs beside the prefix pass)
 // The SM share of a prefix pass that runs first (measured over fourteen
 // copy-on-write shapes on GB300): one unit of its work (a 64-token tile of
 // one 128-row group and KV head) weighs as much as this many MB of the
 // rest-of-context decode's K/V; at this share or above it takes every SM.
-constexpr double kPrefixUnitMB = 0.18;
+constexpr double kPrefixUnitMB = 0.12;
 constexpr double kPrefixAllSmsFrac = 0.85;
 
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -661,8 +661,10 @@ PrefixPlan plan_prefix(const DecodeShape &s, int shared_blocks, int sms, bool tc
             // the SMs in proportion to its work, the rest's bytes at the largest
             // lengths against the pass's (64-token tile x 128-row group x KV
             // head) units, each worth kPrefixUnitMB of rest; all of them when
-            // the rest is small.
-            const double units = static_cast<double>(P / tile) * s.num_kv_heads * pp.tc_groups * s.head_dim / 128.0;
+            // the rest is small. A head_dim 64 unit counts 3/4 of one at 128:
+            // half the products and bytes, the same softmax.
+            const double units = static_cast<double>(P / tile) * s.num_kv_heads * pp.tc_groups *
+                                 (0.5 + 0.5 * s.head_dim / 128.0);
             const double rest_mb = static_cast<double>(s.num_seqs) * std::max<int64_t>(0, s.max_ctx - P) *
                                    s.num_kv_heads * s.head_dim * 4 / 1e6;
             const double frac = units * kPrefixUnitMB / (units * kPrefixUnitMB + rest_mb);

@@ -115,6 +115,14 @@ int TcCfg<D, kGroups>::max_ring_bytes() {
     return room / kStageBytes * kStageBytes;
 }
 
+// A matrix descriptor's start-address field is the byte address / 16 in its
+// low 14 bits; shared-memory addresses stay below 2^18, so the descriptor of
+// base + bytes is the base's plus bytes / 16 (no carry leaves the field).
+// Stepping by constant adds keeps the MMA thread's work per instruction to
+// one add: computed in full each time, the descriptors cost more issue time
+// than the instructions themselves at N = 64.
+__host__ __device__ constexpr uint64_t desc_step(int bytes) { return static_cast<uint64_t>(bytes >> 4); }
+
 __device__ __forceinline__ bool tc_wait(const PrefixParams &p, TcBars *bars, uint64_t *bar, uint32_t parity) {
     if (*reinterpret_cast<volatile int *>(&bars->abort_flag)) return false;
     if (mbar_wait(smem_addr(bar), parity)) return true;
@@ -273,14 +281,17 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             auto issue_pv = [&](int i, int g) -> bool {
                 if (!tc_wait(p, bars, &bars->p_full[g], i & 1)) return false;
                 tc_fence_after();
-                const uint32_t vbase = smem_addr(ring + (i % nstages) * C::kStageBytes) + C::kKBytes;
-                const uint32_t hi = smem_addr(p_hi(g)), lo = smem_addr(p_lo(g));
+                // descriptors of the tile's operands, stepped by constant adds
+                const uint64_t vd = smem_desc_sw128(smem_addr(ring + (i % nstages) * C::kStageBytes) + C::kKBytes,
+                                                    kTcTile * 128, 1024);
+                const uint64_t hd = smem_desc_sw128(smem_addr(p_hi(g)), 16, 1024);
+                const uint64_t ld = smem_desc_sw128(smem_addr(p_lo(g)), 16, 1024);
+                const uint32_t first = i > 0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < kTcTile / 16; ++kk) {
-                    const uint64_t bdesc = smem_desc_sw128(vbase + kk * 16 * 128, kTcTile * 128, 1024);
-                    tc_mma_16bit(tmem + C::o_col(g), smem_desc_sw128(hi + kk * 32, 16, 1024), bdesc, id_pv,
-                                (i > 0 || kk > 0) ? 1u : 0u);
-                    tc_mma_16bit(tmem + C::o_col(g), smem_desc_sw128(lo + kk * 32, 16, 1024), bdesc, id_pv, 1u);
+                    const uint64_t bdesc = vd + desc_step(kk * 16 * 128);
+                    tc_mma_16bit(tmem + C::o_col(g), hd + desc_step(kk * 32), bdesc, id_pv, kk > 0 ? 1u : first);
+                    tc_mma_16bit(tmem + C::o_col(g), ld + desc_step(kk * 32), bdesc, id_pv, 1u);
                 }
                 tc_commit(smem_addr(&bars->pv_done[g]));
                 return true;
@@ -300,14 +311,13 @@ prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
                 for (int g = 0; g < ngrp && ok; ++g) {
                     if (i >= 2 && !tc_wait(p, bars, &bars->s_free[g][b], ((i >> 1) - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t qg = q_base + g * C::kQBytes;
+                    const uint64_t qd = smem_desc_sw128(q_base + g * C::kQBytes, 16, 1024);
+                    const uint64_t kd = smem_desc_sw128(kbase, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t half = kk / 4, off = (kk % 4) * 32;
-                        tc_mma_16bit(tmem + C::s_col(g, b),
-                                    smem_desc_sw128(qg + half * (kTcLanes * 128) + off, 16, 1024),
-                                    smem_desc_sw128(kbase + half * (kTcTile * 128) + off, 16, 1024), id_qk,
-                                    kk > 0 ? 1u : 0u);
+                        const int half = kk / 4, off = (kk % 4) * 32;
+                        tc_mma_16bit(tmem + C::s_col(g, b), qd + desc_step(half * (kTcLanes * 128) + off),
+                                    kd + desc_step(half * (kTcTile * 128) + off), id_qk, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(smem_addr(&bars->s_full[g][b]));
                 }
